@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark of the CP token-layout and owner-gradient-return hot path.
+
+One step = one pass of the whole path over one batch at the pages' training
+shape (CP=4, S=262144 tokens as one causal document, 20 heads x 128, bf16;
+"Add stream-ordered CP gradient return primitive", TransformerEngine PR 3235,
+"Validation"):
+  1. plan: ownership map l2g/g2l and rank-local metadata (2 kernels),
+  2. partition: Q, K and V [S,20,128] into rank-local order (1 kernel),
+  3. grad_return: P=4 writers' global dK and dV [4,S,20,128] summed into the
+     owners' [4,S/4,20,128] in one fused launch (1 kernel).
+Inputs are resident in HBM when the timed region starts; a step touches
+~21.5 GB, far above the 129 MB L2, so no flush is needed between steps.
+
+value = algorithmic bytes of all steps of all ranks / max-over-ranks time.
+Prints ONE JSON line on rank 0. ``--impl reference`` times the CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "grad_return effective HBM GB/s and % of peak (S=262144,P=4); partition tok/s"
+WORKLOAD = "pages-shaped CP=4 step: S=262144 single causal document, 20x128 bf16, DualChunkSwap"
+P, S, H, D = 4, 262144, 20, 128
+ROW_BYTES = H * D * 2
+FALLBACK_HBM_GBS = 6800.0
+
+# Algorithmic bytes (what the method must move), per unit:
+#   grad_return, per owner token (both tensors): 2 x (P reads + 1 write) rows
+#     + 2 int32 index reads
+#   partition, per token (three tensors): 3 x (1 read + 1 write) rows
+#     + 3 int32 index reads
+#   plan, per token: l2g and g2l int32 writes
+GR_BYTES_PER_TOKEN = 2 * (P + 1) * ROW_BYTES + 2 * 4
+PART_BYTES_PER_TOKEN = 3 * 2 * ROW_BYTES + 3 * 4
+PLAN_BYTES_PER_TOKEN = 2 * 4
+
+
+def step_bytes(tokens: int) -> int:
+    return tokens * (GR_BYTES_PER_TOKEN + PART_BYTES_PER_TOKEN + PLAN_BYTES_PER_TOKEN)
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "context_attention_token_gb300", "csrc")
+    for name in ("grad_return.cu", "cpt_device.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, units: int):
+    """DRAM bytes per launch scaled from the committed ncu summary, or None
+    when the summary is missing or was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if "=" in line and not line.startswith("#"):
+                    k, v = line.split("=", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_hash") != kernel_source_hash():
+            return None
+        return int(float(kv["dram_bytes_per_unit"]) * units)
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples = []  # (t, sm, smmax, reasons set)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, smmax = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = []
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                "sw_power_cap"), parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.append(name)
+            self.samples.append((time.time(), sm, smmax, reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        used = inside if inside else self.samples
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({r for s in used for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in used),
+                "sm_max_mhz": max(s[2] for s in used), "reasons": reasons,
+                "samples": len(used), "samples_in_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------- oracle arm
+
+def oracle_sample_step_factory(tokens: int):
+    """One oracle pass of the whole path on `tokens` tokens of the workload
+    (same P, heads, head_dim and layout; a single causal document)."""
+    import numpy as np
+
+    import oracle
+    from context_attention_token_gb300 import synth
+
+    cu = np.array([0, tokens], np.int32)
+    qkv = [synth.normal_bf16(synth.rng_for(3, t), (tokens, H, D)) for t in range(3)]
+    dk = [synth.normal_bf16(synth.rng_for(3, 10 + w), (tokens, H, D), 0.02) for w in range(P)]
+    dv = [synth.normal_bf16(synth.rng_for(3, 20 + w), (tokens, H, D), 0.02) for w in range(P)]
+
+    def step():
+        l2g, _g2l = oracle.index_map(oracle.LAYOUT_DSC, P, cu, tokens)
+        oracle.thd_metadata(oracle.LAYOUT_DSC, P, cu, tokens)
+        for x in qkv:
+            oracle.partition(l2g, x)
+        oracle.grad_return(l2g, dk, oracle.BF16)
+        oracle.grad_return(l2g, dv, oracle.BF16)
+
+    return step
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    tokens = args.sample_tokens
+    if not args.fixed_sample:
+        # size the sample so the whole run takes about args.reference_budget
+        # seconds: time one pass on a small slice, scale per token, round
+        # down to a power of two (a multiple of 2P, as the layout requires)
+        probe = 2048
+        probe_step = oracle_sample_step_factory(probe)
+        probe_step()
+        t0 = time.perf_counter()
+        probe_step()
+        per_token = (time.perf_counter() - t0) / probe
+        fit = args.reference_budget / ((args.steps + args.warmup) * per_token)
+        tokens = 256
+        while tokens * 2 <= min(fit, args.sample_tokens):
+            tokens *= 2
+    step = oracle_sample_step_factory(tokens)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = step_bytes(tokens) * args.steps / dt / 1e9
+    sample = (f"{tokens} of {S} tokens per step (same P=4, 20x128 bf16, single document); "
+              f"whole path: maps, metadata, 3-tensor partition, dK+dV grad_return")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "P": P, "S": S, "H": H, "D": D, "sample_tokens": tokens},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(tokens: int, budget_s: float):
+    step = oracle_sample_step_factory(tokens)
+    step()  # warm caches and page in the inputs
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        step()
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s:
+            break
+    return {"value": step_bytes(tokens) * reps / dt / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": (f"{reps} oracle passes of the whole path over {tokens} of {S} tokens "
+                       f"(same P=4, 20x128 bf16 single document), {dt:.1f} s single-threaded")}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from context_attention_token_gb300 import build as cpt_build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    if rank == 0 or world == 1:
+        cpt_build.build()
+    if world > 1:
+        dist.barrier()
+    from context_attention_token_gb300 import cpt, synth
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+
+    # inputs resident in HBM (seeded device draws)
+    qkv = [synth.device_normal_bf16((S, H, D), 3000 + t, 1.0, dev) for t in range(3)]
+    dkw = synth.device_normal_bf16((P, S, H, D), 3010, 0.02, dev)
+    dvw = synth.device_normal_bf16((P, S, H, D), 3011, 0.02, dev)
+    part = [torch.empty((P, S // P, H, D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    dko = torch.empty((P, S // P, H, D), dtype=torch.bfloat16, device=dev)
+    dvo = torch.empty_like(dko)
+    cu = [0, S]
+    ws = torch.empty(cpt.cpt_plan_workspace_bytes(0, P, 1, S), dtype=torch.uint8, device=dev)
+    kernels_per_step = 4
+
+    ev_gr = []
+    ev_part = []
+
+    def step(record=False):
+        plan = cpt.cpt_plan_create(cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP, P, cu, S, workspace=ws)
+        if record:
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+        cpt.cpt_partition(plan, qkv, part)
+        if record:
+            e1.record(stream)
+        cpt.cpt_grad_return(plan, dkw, dvw, dko, dvo)
+        if record:
+            e2.record(stream)
+            ev_part.append((e0, e1))
+            ev_gr.append((e1, e2))
+        cpt.cpt_plan_destroy(plan)
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not gpu_uuid.startswith("GPU-"):
+            gpu_uuid = "GPU-" + gpu_uuid
+    except Exception:
+        gpu_uuid = str(local)
+    sampler = ClockSampler(gpu_uuid)
+    sampler.start()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    start.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    elapsed_ms = start.elapsed_time(end)
+    gr_ms = [a.elapsed_time(b) for a, b in ev_gr]
+    part_ms = [a.elapsed_time(b) for a, b in ev_part]
+
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in qkv + [dkw, dvw]]
+        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in part + [dko, dvo]]
+        for h, d in zip(host_in, qkv + [dkw, dvw]):
+            h.copy_(d)
+        dev_in = qkv + [dkw, dvw]
+        dev_out = part + [dko, dvo]
+        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+
+        def e2e_step():
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            for h, d in zip(host_out, dev_out):
+                h.copy_(d, non_blocking=True)
+
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        te = torch.tensor([a.elapsed_time(b)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e_ms = float(te.item()) / e2e_steps
+        e2e = {"value": step_bytes(S) * world / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "steps": e2e_steps}
+        del host_in, host_out
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_src = load_peak()
+    gr_bytes = S * GR_BYTES_PER_TOKEN
+    gr_mean_ms = statistics.mean(gr_ms)
+    gr_gbs = gr_bytes / (gr_mean_ms / 1e3) / 1e9
+    part_bytes = S * PART_BYTES_PER_TOKEN
+    part_mean_ms = statistics.mean(part_ms)
+    part_gbs = part_bytes / (part_mean_ms / 1e3) / 1e9
+    value = step_bytes(S) * args.steps * world / (max_ms / 1e3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded device N(0,1) Q/K/V, N(0,0.02) dK/dV)",
+        "config": {"workload": WORKLOAD, "P": P, "S": S, "H": H, "D": D,
+                   "layout": "dual_chunk_swap", "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (21.5 GB touched per step), no flush",
+                   "step_bytes": step_bytes(S)},
+        "grad_return": {"gbs": gr_gbs, "frac_of_peak": gr_gbs / peak, "ms": gr_mean_ms,
+                        "bytes_per_launch": gr_bytes},
+        "partition": {"tok_s": S / (part_mean_ms / 1e3), "gbs": part_gbs,
+                      "frac_of_peak": part_gbs / peak, "ms": part_mean_ms},
+        "roofline": {"kernel": "grad_return", "bound": "hbm", "achieved": gr_gbs, "peak": peak,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6800 GB/s", "unit": "GB/s", "frac": gr_gbs / peak,
+                     "traffic": profiled_traffic("grad_return", S)},
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "gpu_launches": kernels_per_step * args.steps,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.sample_tokens, args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sample-tokens", type=int, default=16384,
+                    help="tokens of the workload the CPU oracle processes per pass")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--reference-budget", type=float, default=120.0,
+                    help="target seconds for a whole --impl reference run")
+    ap.add_argument("--fixed-sample", action="store_true",
+                    help="--impl reference: use --sample-tokens as given")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

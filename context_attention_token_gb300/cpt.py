@@ -1,0 +1,361 @@
+"""Python binding of the C ABI in include/cpt.h (argument marshalling only).
+
+Every function has the name of the C call it wraps. Tensors are torch CUDA
+tensors; the binding turns them into device pointers, passes the current
+torch stream (or the one given), and raises ``CptError`` on any non-zero
+status with the library's message. ctypes releases the GIL for the length of
+each call, as the pages' binding does ("Add stream-ordered CP gradient
+return primitive", TransformerEngine PR 3235, "Greptile Summary": the
+function is registered with a GIL-release guard).
+
+The shared library must have been built (``context_attention_token_gb300.build``);
+importing this module without it raises ImportError: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libcpt.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"{_LIB_PATH} is missing: build it with `python -m context_attention_token_gb300.build` "
+        "(the CUDA path has no fallback)")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+# ------------------------------------------------------------------ constants
+CPT_OK = 0
+CPT_ERR_INVALID_ARG = 1
+CPT_ERR_NOT_DIVISIBLE = 2
+CPT_ERR_UNSUPPORTED = 3
+CPT_ERR_ALIAS = 4
+CPT_ERR_DEVICE = 5
+CPT_ERR_ALIGNMENT = 6
+CPT_ERR_TIMEOUT = 7
+CPT_ERR_CUDA = 8
+CPT_ERR_WORKSPACE = 9
+CPT_ERR_NOT_PUBLISHED = 10
+
+CPT_LAYOUT_DUAL_CHUNK_SWAP = 0
+CPT_LAYOUT_PACKED_CONTIGUOUS = 1
+CPT_F32 = 0
+CPT_BF16 = 1
+CPT_WAIT_BOUNDED = 0
+CPT_WAIT_DRIVER = 1
+CPT_MAX_CP_SIZE = 8
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_u64 = ctypes.c_uint64
+_sz = ctypes.c_size_t
+
+
+def _sig(name, res, *args):
+    f = getattr(_lib, name)
+    f.restype = res
+    f.argtypes = list(args)
+    return f
+
+
+_sig("cpt_last_error_string", ctypes.c_char_p)
+_sig("cpt_status_string", ctypes.c_char_p, ctypes.c_int)
+_sig("cpt_validate_layout", ctypes.c_int, ctypes.c_int, _i32, _vp, _i32, _i64)
+_sig("cpt_plan_workspace_bytes", _sz, ctypes.c_int, _i32, _i32, _i64)
+_sig("cpt_plan_create", ctypes.c_int, ctypes.c_int, _i32, _vp, _i32, _i64, _vp, _sz, _vp,
+     ctypes.POINTER(_vp))
+_sig("cpt_plan_destroy", ctypes.c_int, _vp)
+_sig("cpt_plan_info", ctypes.c_int, _vp, ctypes.POINTER(_i64), ctypes.POINTER(_i32), ctypes.POINTER(_i32))
+_sig("cpt_index_map", ctypes.c_int, _vp, _vp, _vp, _vp)
+_sig("cpt_thd_metadata", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
+_sig("cpt_partition", ctypes.c_int, _vp, _i32, _vp, _vp, _i64, ctypes.c_int, _vp)
+_sig("cpt_grad_return", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, ctypes.c_int, ctypes.c_int, _vp)
+_sig("cpt_grad_scatter", ctypes.c_int, _vp, _i32, _vp, _vp, _vp, _i64, ctypes.c_int, _vp)
+_sig("cpt_epoch_create", ctypes.c_int, _i32, _vp, _vp, _vp, ctypes.POINTER(_vp))
+_sig("cpt_epoch_destroy", ctypes.c_int, _vp)
+_sig("cpt_epoch_advance", ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_uint32))
+_sig("cpt_epoch_publish", ctypes.c_int, _vp, _i32, _vp)
+_sig("cpt_epoch_wait", ctypes.c_int, _vp, _i32, _u64, ctypes.c_int, _vp)
+_sig("cpt_epoch_status", ctypes.c_int, _vp, _i32, _vp, ctypes.POINTER(_i32))
+_sig("cpt_slot_reduce", ctypes.c_int, _vp, _i32, _i64, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def exported_symbols(names):
+    """Names (of the given ones) the loaded library exports."""
+    out = []
+    for n in names:
+        try:
+            getattr(_lib, n)
+            out.append(n)
+        except AttributeError:
+            pass
+    return out
+
+
+class CptError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        name = _lib.cpt_status_string(status).decode()
+        super().__init__(f"{name}: {message}")
+
+
+def _check(status: int):
+    if status != CPT_OK:
+        raise CptError(status, _lib.cpt_last_error_string().decode())
+
+
+def cpt_last_error_string() -> str:
+    return _lib.cpt_last_error_string().decode()
+
+
+def cpt_status_string(status: int) -> str:
+    return _lib.cpt_status_string(status).decode()
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return CPT_F32
+    if t.dtype == torch.bfloat16:
+        return CPT_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _ptr_array(items):
+    arr = (_vp * len(items))(*[_ptr(x) for x in items])
+    return arr
+
+
+def _split(t, parts: int):
+    """A [parts, ...] tensor or a sequence of parts tensors -> list of parts."""
+    if isinstance(t, torch.Tensor):
+        if t.shape[0] != parts:
+            raise ValueError(f"leading dimension {t.shape[0]} != {parts}")
+        return [t[i] for i in range(parts)]
+    t = list(t)
+    if len(t) != parts:
+        raise ValueError(f"expected {parts} tensors, got {len(t)}")
+    return t
+
+
+def _cu_array(cu_seqlens):
+    vals = [int(v) for v in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+    return (_i32 * len(vals))(*vals), len(vals) - 1
+
+
+# ------------------------------------------------------------------ host-only
+
+def cpt_validate_layout(layout: int, cp_size: int, cu_seqlens, total_tokens: int) -> int:
+    """Status code of the host-side partition check (0 = valid)."""
+    arr, n = _cu_array(cu_seqlens)
+    return _lib.cpt_validate_layout(layout, cp_size, ctypes.cast(arr, _vp), n, total_tokens)
+
+
+def cpt_plan_workspace_bytes(layout: int, cp_size: int, n_docs: int, total_tokens: int) -> int:
+    return int(_lib.cpt_plan_workspace_bytes(layout, cp_size, n_docs, total_tokens))
+
+
+# ------------------------------------------------------------------ plan
+
+class Plan:
+    """Host handle of a plan plus the workspace tensor it lives in."""
+
+    def __init__(self, handle: int, workspace: torch.Tensor, layout: int, cp_size: int,
+                 n_docs: int, total_tokens: int):
+        self.handle = handle
+        self.workspace = workspace
+        self.layout = layout
+        self.cp_size = cp_size
+        self.n_docs = n_docs
+        self.total_tokens = total_tokens
+
+    @property
+    def local_tokens(self) -> int:
+        return self.total_tokens // self.cp_size
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h:
+            _lib.cpt_plan_destroy(h)
+
+
+def cpt_plan_create(layout: int, cp_size: int, cu_seqlens, total_tokens: int,
+                    workspace: torch.Tensor | None = None, stream=None) -> Plan:
+    arr, n = _cu_array(cu_seqlens)
+    need = cpt_plan_workspace_bytes(layout, cp_size, n, total_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    h = _vp()
+    _check(_lib.cpt_plan_create(layout, cp_size, ctypes.cast(arr, _vp), n, total_tokens,
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _stream(stream), ctypes.byref(h)))
+    return Plan(h.value, workspace, layout, cp_size, n, total_tokens)
+
+
+def cpt_plan_destroy(plan: Plan) -> None:
+    h, plan.handle = plan.handle, None
+    if h:
+        _check(_lib.cpt_plan_destroy(h))
+
+
+def cpt_plan_info(plan: Plan):
+    """(total_tokens, cp_size, n_docs) as the library holds them."""
+    T, P, n = _i64(), _i32(), _i32()
+    _check(_lib.cpt_plan_info(plan.handle, ctypes.byref(T), ctypes.byref(P), ctypes.byref(n)))
+    return T.value, P.value, n.value
+
+
+def cpt_index_map(plan: Plan, l2g: torch.Tensor, g2l: torch.Tensor | None = None, stream=None):
+    _check(_lib.cpt_index_map(plan.handle, _ptr(l2g), _ptr(g2l), _stream(stream)))
+
+
+def cpt_thd_metadata(plan: Plan, num_segs, seg_doc_first, cu_local, seg_offsets, stream=None):
+    _check(_lib.cpt_thd_metadata(plan.handle, _ptr(num_segs), _ptr(seg_doc_first), _ptr(cu_local),
+                                 _ptr(seg_offsets), _stream(stream)))
+
+
+def cpt_partition(plan: Plan, srcs, dsts, stream=None):
+    """dsts[t] ([P, T/P, ...]) = rank-local reorder of srcs[t] ([T, ...])."""
+    srcs, dsts = list(srcs), list(dsts)
+    if len(srcs) != len(dsts):
+        raise ValueError("srcs and dsts differ in length")
+    _check(_lib.cpt_partition(plan.handle, len(srcs), ctypes.cast(_ptr_array(srcs), _vp),
+                              ctypes.cast(_ptr_array(dsts), _vp), _row_elems(srcs[0]), _dtype_code(srcs[0]),
+                              _stream(stream)))
+
+
+def _row_elems(t: torch.Tensor) -> int:
+    """Elements of one token row of a [T, ...] tensor."""
+    n = 1
+    for d in t.shape[1:]:
+        n *= int(d)
+    return n
+
+
+def cpt_grad_return(plan: Plan, dk_writers, dv_writers, dk_owners, dv_owners, stream=None):
+    """Owners' local dK (and dV) = ordered sum over writers' global gradients.
+
+    Each of the four arguments is a [P, ...] tensor or a list of P tensors;
+    the dV pair may be None.
+    """
+    P = plan.cp_size
+    dkw = _split(dk_writers, P)
+    dko = _split(dk_owners, P)
+    dvw = _split(dv_writers, P) if dv_writers is not None else None
+    dvo = _split(dv_owners, P) if dv_owners is not None else None
+    row = _row_elems(dkw[0])
+    _check(_lib.cpt_grad_return(
+        plan.handle, ctypes.cast(_ptr_array(dkw), _vp),
+        ctypes.cast(_ptr_array(dvw), _vp) if dvw is not None else None,
+        ctypes.cast(_ptr_array(dko), _vp),
+        ctypes.cast(_ptr_array(dvo), _vp) if dvo is not None else None,
+        row, _dtype_code(dkw[0]), _dtype_code(dko[0]), _stream(stream)))
+
+
+def cpt_grad_scatter(plan: Plan, writer: int, src: torch.Tensor, slots, self_slot, stream=None):
+    """slots[o] ([T/P, ...]) = writer's rows owned by o; self_slot must be slots[writer]."""
+    P = plan.cp_size
+    sl = _split(slots, P)
+    _check(_lib.cpt_grad_scatter(plan.handle, writer, _ptr(src), ctypes.cast(_ptr_array(sl), _vp),
+                                 _ptr(self_slot), _row_elems(src), _dtype_code(src),
+                                 _stream(stream)))
+
+
+def cpt_slot_reduce(slots, dst: torch.Tensor, status: torch.Tensor | int | None = None, stream=None):
+    sl = list(slots) if not isinstance(slots, torch.Tensor) else [slots[i] for i in range(slots.shape[0])]
+    _check(_lib.cpt_slot_reduce(ctypes.cast(_ptr_array(sl), _vp), len(sl), sl[0].numel(),
+                                _dtype_code(sl[0]), _dtype_code(dst), _ptr(dst), _ptr(status),
+                                _stream(stream)))
+
+
+# ------------------------------------------------------------------ epochs
+
+class Epoch:
+    def __init__(self, handle: int, flags: torch.Tensor, status: torch.Tensor, cp_size: int):
+        self.handle = handle
+        self.flags = flags
+        self.status = status
+        self.cp_size = cp_size
+
+    def status_ptr(self, owner: int) -> int:
+        return self.status.data_ptr() + 4 * owner
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h:
+            _lib.cpt_epoch_destroy(h)
+
+
+def cpt_epoch_create(cp_size: int, flags: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                     stream=None) -> Epoch:
+    if flags is None:
+        flags = torch.zeros(cp_size * cp_size, dtype=torch.int32, device="cuda")
+    if status is None:
+        status = torch.zeros(cp_size, dtype=torch.int32, device="cuda")
+    h = _vp()
+    _check(_lib.cpt_epoch_create(cp_size, _ptr(flags), _ptr(status), _stream(stream), ctypes.byref(h)))
+    return Epoch(h.value, flags, status, cp_size)
+
+
+def cpt_epoch_destroy(ep: Epoch) -> None:
+    h, ep.handle = ep.handle, None
+    if h:
+        _check(_lib.cpt_epoch_destroy(h))
+
+
+def cpt_epoch_advance(ep: Epoch) -> int:
+    e = ctypes.c_uint32()
+    _check(_lib.cpt_epoch_advance(ep.handle, ctypes.byref(e)))
+    return e.value
+
+
+def cpt_epoch_publish(ep: Epoch, writer: int, stream=None) -> None:
+    _check(_lib.cpt_epoch_publish(ep.handle, writer, _stream(stream)))
+
+
+def cpt_epoch_wait(ep: Epoch, owner: int, timeout_ns: int = 1_000_000_000,
+                   mode: int = CPT_WAIT_BOUNDED, stream=None) -> None:
+    _check(_lib.cpt_epoch_wait(ep.handle, owner, timeout_ns, mode, _stream(stream)))
+
+
+def cpt_epoch_status(ep: Epoch, owner: int, stream=None) -> int:
+    v = _i32()
+    _check(_lib.cpt_epoch_status(ep.handle, owner, _stream(stream), ctypes.byref(v)))
+    return v.value
+
+
+def declared_functions(header_path: str) -> list[str]:
+    """Function names declared in a C header (for the export check)."""
+    with open(header_path) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cpt_[a-z0-9_]+)\s*\(", text)))

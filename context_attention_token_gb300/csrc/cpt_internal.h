@@ -1,0 +1,76 @@
+// Internal launch interface between the C-ABI layer (cpt_api.cu) and the
+// kernels. Not installed; callers use include/cpt.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cpt {
+
+constexpr int kMaxCp = 8;        // largest cp_size (one pointer slot per rank)
+constexpr int kMaxTensors = 3;   // Q, K, V in one gather launch
+
+enum Layout : int { kDualChunkSwap = 0, kPackedContiguous = 1 };
+enum Dtype : int { kF32 = 0, kBf16 = 1 };
+
+// Status codes a kernel may write to a device status word (mirror cpt.h).
+constexpr int32_t kStatusTimeout = 7;
+constexpr int32_t kStatusNotPublished = 10;
+
+// Multiprocessor count of a device (queried once, cached).
+int sm_count(int device);
+
+// a1/a2: l2g[q] and, when g2l != nullptr, g2l[l2g[q]] = q for q in [0, T).
+cudaError_t launch_index_map(int layout, int cp_size, const int32_t *cu, int n_docs, int64_t T,
+                             int32_t *l2g, int32_t *g2l, cudaStream_t stream);
+
+// a3: num_segs[P], seg_doc_first[P], cu_local[P][n+1], seg_offsets[P+1].
+cudaError_t launch_thd_metadata(int layout, int cp_size, const int32_t *cu, int n_docs,
+                                int64_t T, int32_t *num_segs, int32_t *seg_doc_first,
+                                int32_t *cu_local, int32_t *seg_offsets, cudaStream_t stream);
+
+// a4/a6: dst[t][r][j] = src[t][l2g[r*Tp + j]] (bit copy of 16-byte units).
+struct GatherParams {
+    const int32_t *l2g;                  // nullptr: identity map
+    const uint8_t *src[kMaxTensors];     // [T][row_bytes]
+    uint8_t *dst[kMaxTensors][kMaxCp];   // per tensor, per rank: [Tp][row_bytes]
+    int64_t T;
+    int64_t Tp;
+    int64_t rows;        // n_tensors * T
+    int32_t units;       // 16-byte units per row
+    int32_t row_bytes;
+};
+cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream);
+
+// a5: fused owner-gradient return for one or two tensors (dK, dV).
+struct GradReturnParams {
+    const int32_t *l2g;              // [T]
+    const uint8_t *w[2][kMaxCp];     // writer w's global gradient [T][in_row_bytes]
+    uint8_t *o[2][kMaxCp];           // owner o's local gradient [Tp][out_row_bytes]
+    int64_t T;
+    int64_t Tp;
+    int64_t rows;          // n_tensors * T
+    int32_t units;         // 16-byte input units per row
+    int32_t in_row_bytes;
+    int32_t out_row_bytes;
+};
+cudaError_t launch_grad_return(const GradReturnParams &p, int cp_size, int in_dtype,
+                               int out_dtype, cudaStream_t stream);
+
+// a7: dst[i] = ordered binary32 sum of slot_0..slot_{n-1}[i].
+struct SlotReduceParams {
+    const uint8_t *s[kMaxCp];
+    uint8_t *dst;
+    int64_t n_elems;
+    const int32_t *status;   // skip all work when non-null and *status != 0
+};
+cudaError_t launch_slot_reduce(const SlotReduceParams &p, int n_slots, int in_dtype,
+                               int out_dtype, cudaStream_t stream);
+
+// Bounded epoch check: one warp polls flags_row[0..P) with acquire loads until
+// every (int32)(flag - epoch) >= 0, for at most timeout_ns, then writes 0 or
+// kStatusTimeout to *status.
+cudaError_t launch_epoch_check(const uint32_t *flags_row, int cp_size, uint32_t epoch,
+                               uint64_t timeout_ns, int32_t *status, cudaStream_t stream);
+
+}  // namespace cpt

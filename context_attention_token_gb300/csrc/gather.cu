@@ -1,0 +1,77 @@
+// Row gather into rank-local order: the Q/K/V reorder of "[PyTorch] Add
+// experimental packed-contiguous THD all-gather CP" (TransformerEngine PR
+// 3221, commit "Reuse the existing THD CUDA partition and reorder kernels
+// ...") and the per-writer scatter into owner slots of "Add stream-ordered CP
+// gradient return primitive" (TransformerEngine PR 3235, sequence diagram).
+//
+// HBM-bound bit copy: every output row is one source row. A warp owns one row
+// at a time and moves it in 16-byte units, kUnroll units per lane in flight
+// before the first store, so a full SM keeps ~kUnroll * 16 B * 2048 threads of
+// loads outstanding. Rows are visited in output order by a grid-stride loop,
+// so concurrently active warps read and write neighbouring rows.
+#include "cpt_device.cuh"
+#include "cpt_internal.h"
+
+namespace cpt {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+__global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+    const int units = p.units;
+
+    for (int64_t R = warp; R < p.rows; R += nwarps) {
+        const int t = (R >= p.T) + (R >= 2 * p.T);
+        const int64_t q = R - t * p.T;
+        const int r = (int)(q / p.Tp);
+        const int64_t j = q - (int64_t)r * p.Tp;
+        const int64_t g = p.l2g ? (int64_t)__ldg(p.l2g + q) : q;
+        const uint8_t *src = p.src[t] + g * p.row_bytes;
+        uint8_t *dst = p.dst[t][r] + j * p.row_bytes;
+
+        for (int u0 = lane; u0 < units; u0 += 32 * kUnroll) {
+            uint4 v[kUnroll];
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                const int u = u0 + 32 * k;
+                if (u < units) v[k] = ld_once(src + (int64_t)u * 16);
+            }
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                const int u = u0 + 32 * k;
+                if (u < units) st_once(dst + (int64_t)u * 16, v[k]);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream)
+{
+    if (p.rows == 0) return cudaSuccess;
+    static thread_local int cached_dev = -1, cached_blocks = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev != cached_dev) {
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel,
+                                                                      kThreads, 0);
+        if (e != cudaSuccess) return e;
+        cached_blocks = per_sm * sm_count(dev);
+        cached_dev = dev;
+    }
+    const int64_t warps_needed = p.rows;
+    int64_t blocks = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
+    if (blocks > cached_blocks) blocks = cached_blocks;
+    gather_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace cpt

@@ -1,0 +1,358 @@
+/*
+ * cpt.h - C ABI of the context-parallel (CP) token layout and owner-gradient
+ * return library for GB300 (sm_103a).
+ *
+ * The library models the P context-parallel ranks of one CP group as P slot
+ * buffers in the HBM of ONE GPU. It computes
+ *   - the two token ownership policies and their inverses,
+ *   - the rank-local THD sequence metadata,
+ *   - the Q/K/V reorder into rank-local order,
+ *   - the fused owner-gradient return (P writers' global dK/dV summed into
+ *     the owners' local gradients in binary32, writer order 0..P-1),
+ *   - the staged alternative (scatter, epoch publish, bounded epoch wait,
+ *     slot reduce), and the ordered one-shot sum of P slot buffers.
+ *
+ * Sources, by page title:
+ *   [TE-3221] "[PyTorch] Add experimental packed-contiguous THD all-gather
+ *             CP" (TransformerEngine PR 3221): "Why", "Scope and
+ *             constraints", commit messages.
+ *   [TE-3235] "Add stream-ordered CP gradient return primitive"
+ *             (TransformerEngine PR 3235): "Description", "Greptile
+ *             Summary", the sequence diagram, the author's reply.
+ *   [NVSHMEM] "Low Latency Communication Kernels with NVSHMEM" (GPU MODE
+ *             lecture 87 notes): one-shot all-reduce, exercise 3.
+ *
+ * Conventions that hold for every call:
+ *   Memory      The caller owns every buffer. The library never allocates
+ *               device memory; a plan lives in a caller-provided device
+ *               workspace (the memory-management answer in "Kernel-level
+ *               compute-communication overlapping for CP linear attention
+ *               kernels via nvshmem", cuLA issue 15: buffers whose lifetime
+ *               the caller controls; [TE-3235] "Description": peer tensor
+ *               views are supplied by the caller).
+ *   Pointers    "device" pointers must be device memory of the CURRENT
+ *               device, 16-byte aligned. Host arrays of device pointers are
+ *               read during the call only.
+ *   Streams     `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *               default stream). Every call is asynchronous on it unless
+ *               stated; outputs are valid once the stream reaches the call.
+ *   Errors      Checks run on the host before anything is launched
+ *               ("fail-closed validation boundary", [TE-3235] author's
+ *               reply). On failure nothing is enqueued, the call returns a
+ *               non-zero cpt_status and cpt_last_error_string() explains it.
+ *               Device-side failures (epoch wait timeout) go to a device
+ *               status word. Nothing aborts or traps.
+ *   Threads     Calls are thread-safe; the error string is per thread.
+ *   Layout      A "row" is the H*D elements of one token. Global tensors are
+ *               [T][row]. A rank-major local tensor is [P][T/P][row]: rank
+ *               r's j-th local token is flattened local index q = r*T/P + j.
+ */
+#ifndef CPT_H
+#define CPT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CPT_API __attribute__((visibility("default")))
+#else
+#define CPT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum cpt_status {
+    CPT_OK = 0,
+    CPT_ERR_INVALID_ARG = 1,   /* null, negative, out of range, malformed     */
+    CPT_ERR_NOT_DIVISIBLE = 2, /* a partition divisibility rule fails          */
+    CPT_ERR_UNSUPPORTED = 3,   /* a combination outside the validated scope    */
+    CPT_ERR_ALIAS = 4,         /* outputs overlap, or the self slot mismatches */
+    CPT_ERR_DEVICE = 5,        /* not device memory of the current device      */
+    CPT_ERR_ALIGNMENT = 6,     /* a pointer or row size is not 16-byte aligned */
+    CPT_ERR_TIMEOUT = 7,       /* (device status) epoch wait ran out of time   */
+    CPT_ERR_CUDA = 8,          /* a CUDA runtime or driver call failed         */
+    CPT_ERR_WORKSPACE = 9,     /* workspace too small or misaligned            */
+    CPT_ERR_NOT_PUBLISHED = 10 /* wait before every writer published the epoch */
+} cpt_status;
+
+/* Token ownership policy ([TE-3221] "Why").
+ *  DUAL_CHUNK_SWAP    per document: every document is cut into 2P equal
+ *                     chunks; rank r owns chunks r and 2P-1-r ([TE-3235]
+ *                     author's reply: "owner o receives native sequence
+ *                     chunks o and (2*N-1-o)"), kept in ascending global
+ *                     position, documents in order. Each document length
+ *                     must divide by 2P.
+ *  PACKED_CONTIGUOUS  the whole packed buffer is cut into P equal contiguous
+ *                     chunks, rank r owning the r-th; document boundaries
+ *                     survive only through the metadata. T must divide by P.
+ */
+typedef enum cpt_layout {
+    CPT_LAYOUT_DUAL_CHUNK_SWAP = 0,
+    CPT_LAYOUT_PACKED_CONTIGUOUS = 1
+} cpt_layout;
+
+/* Element types. Sums are always accumulated in binary32. */
+typedef enum cpt_dtype { CPT_F32 = 0, CPT_BF16 = 1 } cpt_dtype;
+
+/* How cpt_epoch_wait orders the owner stream after the writers' publishes.
+ *  BOUNDED  stream-ordered event waits on each writer's publish, then a
+ *           one-warp kernel that re-reads the P flags with acquire loads and
+ *           gives up after timeout_ns (default; can never hang).
+ *  DRIVER   cuStreamWaitValue32(>= epoch) on each flag, as [TE-3235]
+ *           "Description" does, then the same bounded check. The driver wait
+ *           itself has no time limit, so it is only enqueued when every
+ *           writer's publish of this epoch is already enqueued. */
+typedef enum cpt_wait_mode { CPT_WAIT_BOUNDED = 0, CPT_WAIT_DRIVER = 1 } cpt_wait_mode;
+
+typedef struct cpt_plan cpt_plan;   /* opaque: layout, P, T, pointers into the workspace */
+typedef struct cpt_epoch cpt_epoch; /* opaque: epoch counter and publish bookkeeping    */
+
+/* Largest cp_size accepted. */
+#define CPT_MAX_CP_SIZE 8
+
+/* ------------------------------------------------------------------ */
+/* Diagnostics                                                         */
+/* ------------------------------------------------------------------ */
+
+/* Message of the last failing call on this thread ("" if none). The pointer
+ * stays valid until the next call on this thread. */
+CPT_API const char *cpt_last_error_string(void);
+
+/* Static name of a status code. */
+CPT_API const char *cpt_status_string(cpt_status status);
+
+/* ------------------------------------------------------------------ */
+/* Host-only checks (no GPU needed)                                    */
+/* ------------------------------------------------------------------ */
+
+/* Validate a partition request without touching the GPU ([TE-3221] "Why"
+ * and "Scope and constraints"; [TE-3235] author's reply).
+ *  cu_seqlens_host  host int32[n_docs+1]: document boundaries of the packed
+ *                   buffer; must start at 0, never decrease, end at
+ *                   total_tokens. Zero-length documents are allowed.
+ *  Returns CPT_OK; CPT_ERR_INVALID_ARG for cp_size outside 1..8, a bad
+ *  layout, n_docs < 0, total_tokens outside [0, 2^31), or malformed
+ *  cu_seqlens; CPT_ERR_NOT_DIVISIBLE when a document length is not a
+ *  multiple of 2*cp_size (DUAL_CHUNK_SWAP) or total_tokens is not a
+ *  multiple of cp_size (PACKED_CONTIGUOUS). */
+CPT_API cpt_status cpt_validate_layout(cpt_layout layout, int32_t cp_size, const int32_t *cu_seqlens_host,
+                               int32_t n_docs, int64_t total_tokens);
+
+/* Device workspace bytes a plan needs (its maps and metadata), or 0 for
+ * arguments that cpt_validate_layout would reject on size grounds. */
+CPT_API size_t cpt_plan_workspace_bytes(cpt_layout layout, int32_t cp_size, int32_t n_docs,
+                                int64_t total_tokens);
+
+/* ------------------------------------------------------------------ */
+/* Plan: ownership maps and metadata, built once per batch              */
+/* ------------------------------------------------------------------ */
+
+/* Validate the request, then build the ownership maps and the metadata
+ * into `workspace` on `stream` (two kernel launches and one small
+ * host-to-device copy of cu_seqlens). One plan serves every later call, so
+ * partition and gradient return always see the same policy ([TE-3221]
+ * "Scope and constraints": partition and attention must see the same
+ * selection).
+ *  workspace        device, 256-byte aligned, >= cpt_plan_workspace_bytes;
+ *                   owned by the caller, must outlive the plan and every
+ *                   call that uses it.
+ *  out              receives a host-side handle; free it with
+ *                   cpt_plan_destroy (which does not touch the workspace).
+ *  The plan is bound to the current device.
+ *  Errors: those of cpt_validate_layout; CPT_ERR_WORKSPACE; CPT_ERR_DEVICE;
+ *  CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_plan_create(cpt_layout layout, int32_t cp_size, const int32_t *cu_seqlens_host,
+                           int32_t n_docs, int64_t total_tokens, void *workspace,
+                           size_t workspace_bytes, void *stream, cpt_plan **out);
+
+/* Free the host handle (NULL is accepted). Work already enqueued is not
+ * affected. */
+CPT_API cpt_status cpt_plan_destroy(cpt_plan *plan);
+
+/* Total tokens T, cp_size P and document count n of a plan (any may be
+ * NULL). Host only. */
+CPT_API cpt_status cpt_plan_info(const cpt_plan *plan, int64_t *total_tokens, int32_t *cp_size,
+                         int32_t *n_docs);
+
+/* ------------------------------------------------------------------ */
+/* Ownership maps                                                      */
+/* ------------------------------------------------------------------ */
+
+/* Write the local-to-global map and its inverse ([TE-3235] author's reply,
+ * [TE-3221] "Why").
+ *  l2g  device int32[T]: l2g[q] = global token held at flattened local
+ *       index q = r*T/P + j.
+ *  g2l  device int32[T] or NULL: g2l[l2g[q]] = q.
+ *  DUAL_CHUNK_SWAP, document i with m = L_i/(2P) and local offset
+ *  u = j - cu[i]/P inside it: l2g = cu[i] + r*m + u when u < m, else
+ *  cu[i] + (2P-1-r)*m + (u-m). PACKED_CONTIGUOUS: l2g[q] = q (rank-major
+ *  ownership needs no reorder, [TE-3221] commit "Allow relaxed THD
+ *  all-gather ...").
+ *  Errors: CPT_ERR_INVALID_ARG, CPT_ERR_DEVICE, CPT_ERR_ALIGNMENT,
+ *  CPT_ERR_ALIAS (l2g and g2l overlap), CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_index_map(const cpt_plan *plan, int32_t *l2g, int32_t *g2l, void *stream);
+
+/* ------------------------------------------------------------------ */
+/* Rank-local THD metadata                                             */
+/* ------------------------------------------------------------------ */
+
+/* Write each rank's local sequence metadata ([TE-3221] commit "Keep
+ * per-document partitioning as the default ...": one chunk and one
+ * attention step per rank in packed mode, document isolation kept through
+ * sequence metadata). All outputs are device int32.
+ *  num_segs[P]        segments of rank r.
+ *  seg_doc_first[P]   document id of rank r's first segment (-1 if none).
+ *                     In packed mode a segment may start inside its
+ *                     document: its keys start at global cu[doc].
+ *  cu_local[P][n+1]   local segment boundaries of rank r; entries from
+ *                     num_segs[r] on are T/P.
+ *  seg_offsets[P+1]   exclusive prefix sum of num_segs.
+ *  DUAL_CHUNK_SWAP: every rank has all n documents, cu_local = cu/P.
+ *  PACKED_CONTIGUOUS: the non-empty pieces of the documents inside
+ *  [r*T/P, (r+1)*T/P), in document order, offsets relative to r*T/P.
+ *  Errors: as cpt_index_map. */
+CPT_API cpt_status cpt_thd_metadata(const cpt_plan *plan, int32_t *num_segs, int32_t *seg_doc_first,
+                            int32_t *cu_local, int32_t *seg_offsets, void *stream);
+
+/* ------------------------------------------------------------------ */
+/* Q/K/V reorder                                                       */
+/* ------------------------------------------------------------------ */
+
+/* Gather up to three token tensors into rank-local order in one launch
+ * ([TE-3221] commit "Reuse the existing THD CUDA partition and reorder
+ * kernels ..."): dst[t][r][j] = src[t][l2g[r*T/P + j]], a bit copy.
+ *  n_tensors  1..3 (Q, K, V).
+ *  src        host array of n_tensors device pointers, each [T][row].
+ *  dst        host array of n_tensors device pointers, each [P][T/P][row]
+ *             (contiguous rank-major); must not overlap any src or another
+ *             dst.
+ *  row_elems  elements per token row (H*D); row bytes must be a multiple
+ *             of 16.
+ *  Errors: CPT_ERR_INVALID_ARG, CPT_ERR_DEVICE, CPT_ERR_ALIGNMENT,
+ *  CPT_ERR_ALIAS, CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_partition(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
+                         void *const *dst, int64_t row_elems, cpt_dtype dtype, void *stream);
+
+/* ------------------------------------------------------------------ */
+/* Fused owner-gradient return                                         */
+/* ------------------------------------------------------------------ */
+
+/* Sum every writer's global dK (and dV) into each owner's local gradient
+ * in one launch ([TE-3235] "Description": scatter into owner buffers in the
+ * two-chunk CP layout, then accumulate the writer slots, the owner's own
+ * slot included per the sequence diagram's 0..cp_size-1):
+ *   out[o][j] = round(((x_0 + x_1) + x_2) + ... + x_{P-1}),
+ *   x_w = (float) writer_w[l2g[o*T/P + j]],
+ * binary32 adds in writer order with the accumulator starting at x_0, then
+ * one rounding to the output type (round-to-nearest-even for bf16). The
+ * owner buffers are overwritten.
+ *  dk_writers  host array of P device pointers, writer w's global [T][row].
+ *  dk_owners   host array of P device pointers, owner o's local [T/P][row].
+ *  dv_writers, dv_owners  the same for dV, or both NULL to return dK only.
+ *  in, out     element types of writers and owners.
+ *  Errors: CPT_ERR_INVALID_ARG (one of the dV pair NULL), CPT_ERR_DEVICE,
+ *  CPT_ERR_ALIGNMENT, CPT_ERR_ALIAS (an owner buffer overlaps any buffer
+ *  of the call), CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_grad_return(const cpt_plan *plan, const void *const *dk_writers,
+                           const void *const *dv_writers, void *const *dk_owners,
+                           void *const *dv_owners, int64_t row_elems, cpt_dtype in,
+                           cpt_dtype out, void *stream);
+
+/* ------------------------------------------------------------------ */
+/* Staged owner-gradient return: scatter, publish, wait, reduce        */
+/* ------------------------------------------------------------------ */
+
+/* Scatter one writer's global gradient into its slot of every owner
+ * ([TE-3235] sequence diagram, "copy_() scatter dk_global to
+ * peer_grad_key_returns[owner][rank]"): slots[o][j] = src[l2g[o*T/P + j]].
+ *  writer     0..P-1.
+ *  src        device [T][row].
+ *  slots      host array of P device pointers: slots[o] is this writer's
+ *             slot [T/P][row] in owner o's return buffer.
+ *  self_slot  device pointer of the writer's own local slot as the owner
+ *             sees it; must equal slots[writer] (the self-alias assertion
+ *             of [TE-3235] "Greptile Summary"), else CPT_ERR_ALIAS.
+ *  Errors: as cpt_partition, plus CPT_ERR_ALIAS. */
+CPT_API cpt_status cpt_grad_scatter(const cpt_plan *plan, int32_t writer, const void *src,
+                            void *const *slots, const void *self_slot, int64_t row_elems,
+                            cpt_dtype dtype, void *stream);
+
+/* Create the epoch state of one CP group ([TE-3235] "Description": writer
+ * epochs published with cuStreamWriteValue32, waited with
+ * cuStreamWaitValue32; the state is caller-owned instead of the
+ * unpruned static epoch map that "Greptile Summary" flags).
+ *  flags   device uint32[P][P], owner-major: flags[o*P + w] is writer w's
+ *          last published epoch as seen by owner o.
+ *  status  device int32[P]: status[o] is the outcome of owner o's last
+ *          wait (0, CPT_ERR_TIMEOUT or CPT_ERR_NOT_PUBLISHED).
+ *  Zeroes both on `stream`; the epoch counter starts at 0. Creates P CUDA
+ *  events (no device memory). Errors: CPT_ERR_INVALID_ARG, CPT_ERR_DEVICE,
+ *  CPT_ERR_ALIGNMENT (4-byte), CPT_ERR_ALIAS, CPT_ERR_UNSUPPORTED (driver
+ *  stream memory operations unavailable), CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_epoch_create(int32_t cp_size, uint32_t *flags, int32_t *status, void *stream,
+                            cpt_epoch **out);
+
+/* Destroy the host state and its events. Waits for nothing. */
+CPT_API cpt_status cpt_epoch_destroy(cpt_epoch *ep);
+
+/* Start the next epoch: epoch += 1 (0 is skipped on wrap-around). Host
+ * only. `epoch_out` may be NULL. */
+CPT_API cpt_status cpt_epoch_advance(cpt_epoch *ep, uint32_t *epoch_out);
+
+/* Publish the current epoch from `writer` to every owner: P driver stream
+ * writes flags[o*P + writer] = epoch, each ordered after all earlier work
+ * on `stream` (with the driver's default memory barrier), then an event
+ * record. Errors: CPT_ERR_INVALID_ARG (writer out of range, or no epoch
+ * started), CPT_ERR_DEVICE, CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_epoch_publish(cpt_epoch *ep, int32_t writer, void *stream);
+
+/* Make `stream` wait until every writer has published the current epoch to
+ * `owner` ([TE-3235] sequence diagram: wait until all cp_size slots are
+ * >= epoch; the comparison is wrap-around safe, (int32)(flag - epoch) >= 0).
+ *  Host check first: if some writer has not yet enqueued its publish of this
+ *  epoch, nothing waits; status[owner] is set to CPT_ERR_NOT_PUBLISHED on
+ *  `stream` and the call returns CPT_ERR_NOT_PUBLISHED.
+ *  Otherwise `stream` is ordered after the publishes (see cpt_wait_mode),
+ *  and a one-warp kernel re-reads the P flags with acquire loads, polling
+ *  for at most timeout_ns (0 = a single check) and an iteration cap, then
+ *  writes status[owner] = 0 or CPT_ERR_TIMEOUT. Pass `status + owner` to
+ *  cpt_slot_reduce to skip the reduction after a failed wait.
+ *  The writer streams must not depend on work enqueued on `stream` after
+ *  this call. Errors: CPT_ERR_INVALID_ARG, CPT_ERR_NOT_PUBLISHED,
+ *  CPT_ERR_DEVICE, CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_epoch_wait(cpt_epoch *ep, int32_t owner, uint64_t timeout_ns, cpt_wait_mode mode,
+                          void *stream);
+
+/* Synchronise `stream` and read status[owner] into *device_status.
+ * The one blocking call of the library. */
+CPT_API cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *stream,
+                            int32_t *device_status);
+
+/* ------------------------------------------------------------------ */
+/* Ordered slot reduce                                                 */
+/* ------------------------------------------------------------------ */
+
+/* One-shot ordered sum of n_slots equally sized buffers ([TE-3235]
+ * sequence diagram "accumulate grad_key_return[0..cp_size-1]"; [NVSHMEM]
+ * one-shot all-reduce, every element reading all slots in one step):
+ *   dst[i] = round(((s_0[i] + s_1[i]) + ...) + s_{n-1}[i]) in binary32.
+ *  slots     host array of n_slots (1..8) device pointers, each n_elems
+ *            elements of type `in`.
+ *  dst       device, n_elems elements of type `out`; must not overlap a
+ *            slot.
+ *  status    device int32 or NULL; when non-NULL and non-zero at kernel
+ *            start, the kernel writes nothing (a failed epoch wait).
+ *  n_elems   any value >= 0; pointers must be 16-byte aligned.
+ *  Errors: CPT_ERR_INVALID_ARG, CPT_ERR_DEVICE, CPT_ERR_ALIGNMENT,
+ *  CPT_ERR_ALIAS, CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_slot_reduce(const void *const *slots, int32_t n_slots, int64_t n_elems,
+                           cpt_dtype in, cpt_dtype out, void *dst, const int32_t *status,
+                           void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPT_H */
