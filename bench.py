@@ -33,10 +33,13 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "grad_return effective HBM GB/s and % of peak (S=262144,P=4); partition tok/s"
-WORKLOAD = "pages-shaped CP=4 step: S=262144 single causal document, 20x128 bf16, DualChunkSwap"
-P, S, H, D = 4, 262144, 20, 128
-ROW_BYTES = H * D * 2
+def workload() -> str:
+    return (f"{'pages-shaped ' if (S, H) == (262144, 20) else ''}CP=4 step: S={S} single causal "
+            f"document, {H}x{D} bf16, DualChunkSwap")
+P, D = 4, 128
+S, H = 262144, 20  # the pages' shape; --tokens / --heads select a smaller case
 FALLBACK_HBM_GBS = 6800.0
+
 
 # Algorithmic bytes (what the method must move), per unit:
 #   grad_return, per owner token (both tensors): 2 x (P reads + 1 write) rows
@@ -44,13 +47,23 @@ FALLBACK_HBM_GBS = 6800.0
 #   partition, per token (three tensors): 3 x (1 read + 1 write) rows
 #     + 3 int32 index reads
 #   plan, per token: l2g and g2l int32 writes
-GR_BYTES_PER_TOKEN = 2 * (P + 1) * ROW_BYTES + 2 * 4
-PART_BYTES_PER_TOKEN = 3 * 2 * ROW_BYTES + 3 * 4
+def row_bytes() -> int:
+    return H * D * 2
+
+
+def gr_bytes_per_token() -> int:
+    return 2 * (P + 1) * row_bytes() + 2 * 4
+
+
+def part_bytes_per_token() -> int:
+    return 3 * 2 * row_bytes() + 3 * 4
+
+
 PLAN_BYTES_PER_TOKEN = 2 * 4
 
 
 def step_bytes(tokens: int) -> int:
-    return tokens * (GR_BYTES_PER_TOKEN + PART_BYTES_PER_TOKEN + PLAN_BYTES_PER_TOKEN)
+    return tokens * (gr_bytes_per_token() + part_bytes_per_token() + PLAN_BYTES_PER_TOKEN)
 
 
 def load_peak():
@@ -214,7 +227,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "P": P, "S": S, "H": H, "D": D, "sample_tokens": tokens},
+        "config": {"workload": workload(), "P": P, "S": S, "H": H, "D": D, "sample_tokens": tokens},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -374,10 +387,10 @@ def run_gpu(args):
         return 0
 
     peak, peak_src = load_peak()
-    gr_bytes = S * GR_BYTES_PER_TOKEN
+    gr_bytes = S * gr_bytes_per_token()
     gr_mean_ms = statistics.mean(gr_ms)
     gr_gbs = gr_bytes / (gr_mean_ms / 1e3) / 1e9
-    part_bytes = S * PART_BYTES_PER_TOKEN
+    part_bytes = S * part_bytes_per_token()
     part_mean_ms = statistics.mean(part_ms)
     part_gbs = part_bytes / (part_mean_ms / 1e3) / 1e9
     value = step_bytes(S) * args.steps * world / (max_ms / 1e3) / 1e9
@@ -387,7 +400,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded device N(0,1) Q/K/V, N(0,0.02) dK/dV)",
-        "config": {"workload": WORKLOAD, "P": P, "S": S, "H": H, "D": D,
+        "config": {"workload": workload(), "P": P, "S": S, "H": H, "D": D,
                    "layout": "dual_chunk_swap", "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (21.5 GB touched per step), no flush",
                    "step_bytes": step_bytes(S)},
@@ -413,6 +426,7 @@ def run_gpu(args):
 
 
 def main():
+    global S, H
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -428,7 +442,12 @@ def main():
                     help="target seconds for a whole --impl reference run")
     ap.add_argument("--fixed-sample", action="store_true",
                     help="--impl reference: use --sample-tokens as given")
+    ap.add_argument("--tokens", type=int, default=S, help="S (multiple of 2P)")
+    ap.add_argument("--heads", type=int, default=H)
     args = ap.parse_args()
+    S, H = args.tokens, args.heads
+    if S % (2 * P) or S <= 0 or H <= 0:
+        ap.error("--tokens must be a positive multiple of 8, --heads positive")
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
