@@ -103,6 +103,27 @@ def profiled_traffic(kernel: str, units: int):
         return None
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks of the default process group (the value
+    itself without one). Timing uses it so that the slowest replica sets the
+    whole-job time."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """GB/s of the whole job: every replica's bytes over the slowest replica's time."""
+    return bytes_per_step * steps * world / (max_ms / 1e3) / 1e9
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -336,10 +357,7 @@ def run_gpu(args):
     gr_ms = [a.elapsed_time(b) for a, b in ev_gr]
     part_ms = [a.elapsed_time(b) for a, b in ev_part]
 
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
+    max_ms = max_over_ranks(elapsed_ms, dev)
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -371,11 +389,8 @@ def run_gpu(args):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        te = torch.tensor([a.elapsed_time(b)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e_ms = float(te.item()) / e2e_steps
-        e2e = {"value": step_bytes(S) * world / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+        e2e_ms = max_over_ranks(a.elapsed_time(b), dev) / e2e_steps
+        e2e = {"value": whole_job_gbs(step_bytes(S), 1, world, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": e2e_steps}
         del host_in, host_out
@@ -393,7 +408,7 @@ def run_gpu(args):
     part_bytes = S * part_bytes_per_token()
     part_mean_ms = statistics.mean(part_ms)
     part_gbs = part_bytes / (part_mean_ms / 1e3) / 1e9
-    value = step_bytes(S) * args.steps * world / (max_ms / 1e3) / 1e9
+    value = whole_job_gbs(step_bytes(S), args.steps, world, max_ms)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -425,6 +440,78 @@ def run_gpu(args):
     return 0
 
 
+# ---------------------------------------------------------------- slot-reduce sweep
+
+def run_slot_reduce_sweep(args):
+    """P=8 slot buffers of N bytes each, N = 1 KB x 4^k up to 1 GB, float32 and
+    bf16: one ordered sum per launch. One JSON line per (dtype, N), with the
+    launch latency (back-to-back C-ABI calls, and replays of a CUDA graph of
+    such calls) and the effective bandwidth over 9N algorithmic bytes."""
+    import torch
+
+    from context_attention_token_gb300 import build as cpt_build
+
+    cpt_build.build()
+    from context_attention_token_gb300 import cpt
+
+    torch.cuda.set_device(0)
+    peak, peak_src = load_peak()
+    stream = torch.cuda.Stream()
+    n_slots = 8
+    for dtype in (torch.float32, torch.bfloat16):
+        esz = torch.tensor([], dtype=dtype).element_size()
+        for k in range(11):
+            nbytes = 1024 * 4**k
+            n = nbytes // esz
+            gen = torch.Generator(device="cuda")
+            gen.manual_seed(5000 + k)
+            slots = [(torch.rand(n, device="cuda", generator=gen) * 2 - 1).to(dtype) for _ in range(n_slots)]
+            dst = torch.empty(n, dtype=dtype, device="cuda")
+            iters = max(3, min(2000, int(2e9 // (9 * nbytes))))
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    cpt.cpt_slot_reduce(slots, dst, stream=stream)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(iters):
+                    cpt.cpt_slot_reduce(slots, dst, stream=stream)
+                b.record(stream)
+            torch.cuda.synchronize()
+            call_us = a.elapsed_time(b) * 1e3 / iters
+            # the same calls captured once into a graph and replayed
+            graph_us = None
+            g_iters = min(iters, 200)
+            try:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                    for _ in range(g_iters):
+                        cpt.cpt_slot_reduce(slots, dst, stream=torch.cuda.current_stream())
+                g.replay()
+                torch.cuda.synchronize()
+                a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    a2.record(stream)
+                    g.replay()
+                    b2.record(stream)
+                torch.cuda.synchronize()
+                graph_us = a2.elapsed_time(b2) * 1e3 / g_iters
+                del g
+            except Exception as e:  # capture refused: report the plain number only
+                graph_us = f"capture failed: {e}"
+            best_us = min(call_us, graph_us) if isinstance(graph_us, float) else call_us
+            gbs = 9 * nbytes / (best_us * 1e-6) / 1e9
+            line = {"sweep": "slot_reduce", "metric": "slot_reduce latency and effective GB/s",
+                    "dtype": "f32" if dtype == torch.float32 else "bf16", "slots": n_slots,
+                    "bytes_per_slot": nbytes, "iters": iters,
+                    "us_per_call_launched": call_us, "us_per_call_graph": graph_us,
+                    "gbs": gbs, "frac_of_peak": gbs / peak, "peak": peak, "peak_source": peak_src}
+            print(json.dumps(line), flush=True)
+            del slots, dst
+            torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     global S, H
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -442,6 +529,8 @@ def main():
                     help="target seconds for a whole --impl reference run")
     ap.add_argument("--fixed-sample", action="store_true",
                     help="--impl reference: use --sample-tokens as given")
+    ap.add_argument("--sweep", choices=["slot_reduce"], default=None,
+                    help="instead of the step: the slot-reduce message-size sweep")
     ap.add_argument("--tokens", type=int, default=S, help="S (multiple of 2P)")
     ap.add_argument("--heads", type=int, default=H)
     args = ap.parse_args()
@@ -451,6 +540,8 @@ def main():
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep == "slot_reduce":
+        return run_slot_reduce_sweep(args)
     return run_gpu(args)
 
 
