@@ -76,6 +76,8 @@ _sig("cpt_index_map", ctypes.c_int, _vp, _vp, _vp, _vp)
 _sig("cpt_thd_metadata", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("cpt_partition", ctypes.c_int, _vp, _i32, _vp, _vp, _i64, ctypes.c_int, _vp)
 _sig("cpt_grad_return", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, ctypes.c_int, ctypes.c_int, _vp)
+_sig("cpt_grad_return_noalloc", ctypes.c_int, ctypes.c_int, _i32, _vp, _i32, _i64, _vp, _vp, _vp, _vp,
+     _i64, ctypes.c_int, ctypes.c_int, _vp)
 _sig("cpt_grad_scatter", ctypes.c_int, _vp, _i32, _vp, _vp, _vp, _i64, ctypes.c_int, _vp)
 _sig("cpt_epoch_create", ctypes.c_int, _i32, _vp, _vp, _vp, ctypes.POINTER(_vp))
 _sig("cpt_epoch_destroy", ctypes.c_int, _vp)
@@ -279,6 +281,30 @@ def cpt_grad_return(plan: Plan, dk_writers, dv_writers, dk_owners, dv_owners, st
         ctypes.cast(_ptr_array(dko), _vp),
         ctypes.cast(_ptr_array(dvo), _vp) if dvo is not None else None,
         row, _dtype_code(dkw[0]), _dtype_code(dko[0]), _stream(stream)))
+
+
+CPT_NOALLOC_MAX_TOKENS = 1048576
+CPT_NOALLOC_MAX_DOCS = 65536
+
+
+def cpt_grad_return_noalloc(layout: int, cp_size: int, cu_seqlens, total_tokens: int, dk_writers,
+                            dv_writers, dk_owners, dv_owners, stream=None):
+    """cpt_grad_return without a plan or workspace, for callers that cannot
+    allocate device memory: the map lives in a fixed-size array inside the
+    library (at most CPT_NOALLOC_MAX_TOKENS tokens). Calls that overlap on
+    the GPU share that array and race."""
+    arr, n = _cu_array(cu_seqlens)
+    P = cp_size
+    dkw = _split(dk_writers, P)
+    dko = _split(dk_owners, P)
+    dvw = _split(dv_writers, P) if dv_writers is not None else None
+    dvo = _split(dv_owners, P) if dv_owners is not None else None
+    _check(_lib.cpt_grad_return_noalloc(
+        layout, P, ctypes.cast(arr, _vp), n, total_tokens, ctypes.cast(_ptr_array(dkw), _vp),
+        ctypes.cast(_ptr_array(dvw), _vp) if dvw is not None else None,
+        ctypes.cast(_ptr_array(dko), _vp),
+        ctypes.cast(_ptr_array(dvo), _vp) if dvo is not None else None,
+        _row_elems(dkw[0]), _dtype_code(dkw[0]), _dtype_code(dko[0]), _stream(stream)))
 
 
 def cpt_grad_scatter(plan: Plan, writer: int, src: torch.Tensor, slots, self_slot, stream=None):

@@ -743,3 +743,116 @@ cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *stream, in
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------- no allocation
+//
+// Fused gradient return for callers that cannot allocate device memory. Its
+// map scratch is a file-scope device array, sized for at most
+// CPT_NOALLOC_MAX_TOKENS tokens and CPT_NOALLOC_MAX_DOCS documents, which every
+// GPU that loads this library holds until the process exits.
+
+namespace {
+
+constexpr int64_t kNoAllocCuSlots = CPT_NOALLOC_MAX_DOCS + 64;  // keeps the map 256-byte aligned
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocCuSlots + CPT_NOALLOC_MAX_TOKENS];
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current (host code only sees a host-side stand-in under the name).
+cpt_status noalloc_scratch(int device, int32_t **out)
+{
+    static std::mutex mu;
+    static int32_t *addr[64] = {nullptr};
+    if (device < 0 || device >= 64) return fail(CPT_ERR_DEVICE, "device %d out of range", device);
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[device] == nullptr) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return cuda_fail(e, "cudaGetSymbolAddress of the no-allocation scratch");
+        }
+        addr[device] = static_cast<int32_t *>(p);
+    }
+    *out = addr[device];
+    return CPT_OK;
+}
+
+}  // namespace
+
+extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, const int32_t *cu,
+                                              int32_t n, int64_t T, const void *const *dkw,
+                                              const void *const *dvw, void *const *dko,
+                                              void *const *dvo, int64_t row_elems, cpt_dtype in,
+                                              cpt_dtype out, void *stream)
+{
+    cpt_status st = cpt_validate_layout(layout, P, cu, n, T);
+    if (st) return st;
+    if (T > CPT_NOALLOC_MAX_TOKENS)
+        return fail(CPT_ERR_INVALID_ARG,
+                    "total_tokens %lld exceeds the no-allocation limit of %d tokens "
+                    "(use cpt_plan_create with a workspace)",
+                    (long long)T, CPT_NOALLOC_MAX_TOKENS);
+    if (n > CPT_NOALLOC_MAX_DOCS)
+        return fail(CPT_ERR_INVALID_ARG,
+                    "n_docs %d exceeds the no-allocation limit of %d documents "
+                    "(use cpt_plan_create with a workspace)",
+                    n, CPT_NOALLOC_MAX_DOCS);
+    if (dkw == nullptr || dko == nullptr)
+        return fail(CPT_ERR_INVALID_ARG, "dk_writers or dk_owners is NULL");
+    if ((dvw == nullptr) != (dvo == nullptr))
+        return fail(CPT_ERR_INVALID_ARG, "dv_writers and dv_owners must both be given or both NULL");
+    int64_t units = 0;
+    if ((st = check_row(row_elems, in, out, &units))) return st;
+    int dev = 0;
+    if (!current_device(&dev)) return fail(CPT_ERR_CUDA, "cudaGetDevice failed");
+    int32_t *scratch = nullptr;
+    if ((st = noalloc_scratch(dev, &scratch))) return st;
+    if (T == 0) return CPT_OK;
+
+    const int nt = dvw ? 2 : 1;
+    const int64_t Tp = T / P;
+    const int64_t in_row = units * 16;
+    const int64_t out_row = row_elems * (int64_t)dtype_size(out);
+    const void *const *W[2] = {dkw, dvw};
+    void *const *O[2] = {dko, dvo};
+    static const char *wn[2] = {"dk_writers", "dv_writers"};
+    static const char *on[2] = {"dk_owners", "dv_owners"};
+    std::vector<Range> r;
+    add_range(r, scratch, sizeof(int32_t) * (size_t)(kNoAllocCuSlots + CPT_NOALLOC_MAX_TOKENS), false,
+              "scratch");
+    for (int t = 0; t < nt; ++t)
+        for (int w = 0; w < P; ++w) {
+            if ((st = check_ptr(W[t][w], dev, 16, wn[t], w))) return st;
+            if ((st = check_ptr(O[t][w], dev, 16, on[t], w))) return st;
+            add_range(r, W[t][w], (size_t)(T * in_row), false, wn[t], w);
+            add_range(r, O[t][w], (size_t)(Tp * out_row), true, on[t], w);
+        }
+    if ((st = check_overlaps(r))) return st;
+
+    // every entry of the map is rewritten before it is read, so nothing in the
+    // scratch has to start at zero
+    int32_t *d_cu = scratch;
+    int32_t *d_l2g = scratch + kNoAllocCuSlots;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(d_cu, cu, sizeof(int32_t) * (size_t)(n + 1),
+                                    cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = launch_index_map(layout, P, d_cu, n, T, d_l2g, nullptr, s);
+    if (e != cudaSuccess) return cuda_fail(e, "no-allocation map build");
+
+    GradReturnParams p;
+    memset(&p, 0, sizeof p);
+    p.l2g = d_l2g;
+    for (int t = 0; t < nt; ++t)
+        for (int w = 0; w < P; ++w) {
+            p.w[t][w] = static_cast<const uint8_t *>(W[t][w]);
+            p.o[t][w] = static_cast<uint8_t *>(O[t][w]);
+        }
+    p.T = T;
+    p.Tp = Tp;
+    p.rows = (int64_t)nt * T;
+    p.units = (int32_t)units;
+    p.in_row_bytes = (int32_t)in_row;
+    p.out_row_bytes = (int32_t)out_row;
+    e = launch_grad_return(p, P, in, out, s);
+    return e == cudaSuccess ? CPT_OK : cuda_fail(e, "grad_return launch");
+}

@@ -260,6 +260,43 @@ CPT_API cpt_status cpt_grad_return(const cpt_plan *plan, const void *const *dk_w
                            void *const *dv_owners, int64_t row_elems, cpt_dtype in,
                            cpt_dtype out, void *stream);
 
+/* Largest batch cpt_grad_return_noalloc accepts. */
+#define CPT_NOALLOC_MAX_TOKENS 1048576
+#define CPT_NOALLOC_MAX_DOCS 65536
+
+/* The fused gradient return of cpt_grad_return for callers that cannot
+ * allocate device memory. Such callers include a plugin whose host
+ * application owns every device byte through its own pool, and a step whose
+ * memory plan is fixed before it runs. They cannot hand cpt_plan_create a
+ * workspace. The pages have no counterpart to this call; it adds no
+ * arithmetic, only a different home for the ownership map.
+ *
+ * Arguments and results are those of cpt_plan_create (layout, cp_size,
+ * cu_seqlens_host, n_docs, total_tokens) followed by those of
+ * cpt_grad_return; the output is bit-identical to a plan-based call. The map
+ * is built into a file-scope device array inside the library instead of a
+ * workspace, so the call allocates nothing:
+ *  - Limits: total_tokens <= CPT_NOALLOC_MAX_TOKENS and n_docs <=
+ *    CPT_NOALLOC_MAX_DOCS; larger batches are rejected with
+ *    CPT_ERR_INVALID_ARG and a message naming the limit. The array is
+ *    (CPT_NOALLOC_MAX_DOCS + 64 + CPT_NOALLOC_MAX_TOKENS) int32, about 4.5 MB,
+ *    and every GPU that loads the library holds it until the process exits.
+ *  - The first call on a device looks the array's device address up with
+ *    that device current (a one-time set-up that enqueues nothing); make that
+ *    first call before any stream capture.
+ *  - Every call shares the one array and leaves its map there. Calls ordered
+ *    on one stream are safe; calls that overlap on the GPU (two streams, or
+ *    two threads, at once) race on it and may return wrong sums.
+ *  - Nothing in the array needs to start at zero: each call rewrites every
+ *    map entry it reads.
+ *  Errors: those of cpt_validate_layout and cpt_grad_return. */
+CPT_API cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t cp_size,
+                                           const int32_t *cu_seqlens_host, int32_t n_docs,
+                                           int64_t total_tokens, const void *const *dk_writers,
+                                           const void *const *dv_writers, void *const *dk_owners,
+                                           void *const *dv_owners, int64_t row_elems,
+                                           cpt_dtype in, cpt_dtype out, void *stream);
+
 /* ------------------------------------------------------------------ */
 /* Staged owner-gradient return: scatter, publish, wait, reduce        */
 /* ------------------------------------------------------------------ */
