@@ -457,6 +457,7 @@ def run_slot_reduce_sweep(args):
     torch.cuda.set_device(0)
     peak, peak_src = load_peak()
     stream = torch.cuda.Stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     n_slots = 8
     for dtype in (torch.float32, torch.bfloat16):
         esz = torch.tensor([], dtype=dtype).element_size()
@@ -499,12 +500,25 @@ def run_slot_reduce_sweep(args):
                 del g
             except Exception as e:  # capture refused: report the plain number only
                 graph_us = f"capture failed: {e}"
-            best_us = min(call_us, graph_us) if isinstance(graph_us, float) else call_us
-            gbs = 9 * nbytes / (best_us * 1e-6) / 1e9
+            # each call alone after an L2 flush (a 512 MB write): DRAM-honest
+            cold = []
+            with torch.cuda.stream(stream):
+                for _ in range(min(iters, 20)):
+                    flush.zero_()
+                    a3, b3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a3.record(stream)
+                    cpt.cpt_slot_reduce(slots, dst, stream=stream)
+                    b3.record(stream)
+                    cold.append((a3, b3))
+            torch.cuda.synchronize()
+            cold_us = statistics.median(a3.elapsed_time(b3) for a3, b3 in cold) * 1e3
+            gbs = 9 * nbytes / (cold_us * 1e-6) / 1e9
             line = {"sweep": "slot_reduce", "metric": "slot_reduce latency and effective GB/s",
                     "dtype": "f32" if dtype == torch.float32 else "bf16", "slots": n_slots,
                     "bytes_per_slot": nbytes, "iters": iters,
                     "us_per_call_launched": call_us, "us_per_call_graph": graph_us,
+                    "us_per_call_cold_l2": cold_us,
+                    "l2_resident_when_repeated": 9 * nbytes < 129 * 2**20,
                     "gbs": gbs, "frac_of_peak": gbs / peak, "peak": peak, "peak_source": peak_src}
             print(json.dumps(line), flush=True)
             del slots, dst
