@@ -33,12 +33,14 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "grad_return effective HBM GB/s and % of peak (S=262144,P=4); partition tok/s"
-def workload() -> str:
-    return (f"{'pages-shaped ' if (S, H) == (262144, 20) else ''}CP=4 step: S={S} single causal "
-            f"document, {H}x{D} bf16, DualChunkSwap")
 P, D = 4, 128
 S, H = 262144, 20  # the pages' shape; --tokens / --heads select a smaller case
 FALLBACK_HBM_GBS = 6800.0
+
+
+def workload() -> str:
+    return (f"{'pages-shaped ' if (S, H) == (262144, 20) else ''}CP=4 step: S={S} single causal "
+            f"document, {H}x{D} bf16, DualChunkSwap")
 
 
 # Algorithmic bytes (what the method must move), per unit:
@@ -51,7 +53,14 @@ def row_bytes() -> int:
     return H * D * 2
 
 
+PATH = "fused"
+
+
 def gr_bytes_per_token() -> int:
+    if PATH == "staged":
+        # per token and tensor: P writers read and write their row into a slot,
+        # then the owner reads P slot rows and writes one; plus P index reads
+        return 2 * ((3 * P + 1) * row_bytes() + P * 4)
     return 2 * (P + 1) * row_bytes() + 2 * 4
 
 
@@ -319,12 +328,47 @@ def run_gpu(args):
         cpt.cpt_partition(plan, qkv, part)
         if record:
             e1.record(stream)
-        cpt.cpt_grad_return(plan, dkw, dvw, dko, dvo)
+        if args.path == "staged":
+            grad_return_staged(plan)
+        else:
+            cpt.cpt_grad_return(plan, dkw, dvw, dko, dvo)
         if record:
             e2.record(stream)
             ev_part.append((e0, e1))
             ev_gr.append((e1, e2))
         cpt.cpt_plan_destroy(plan)
+
+    if args.path == "staged":
+        # P writer streams scatter their global dK/dV into owner-major slots
+        # [owner][writer] and publish the epoch; P owner streams wait for all
+        # writers and reduce their P slots in writer order.
+        slots_k = torch.empty((P, P, S // P, H, D), dtype=torch.bfloat16, device=dev)
+        slots_v = torch.empty_like(slots_k)
+        ep = cpt.cpt_epoch_create(P)
+        wstreams = [torch.cuda.Stream() for _ in range(P)]
+        ostreams = [torch.cuda.Stream() for _ in range(P)]
+        kernels_per_step = 2 + 1 + P * 2 + P * 3  # plan, partition, scatters, checks + reduces
+
+    def grad_return_staged(plan):
+        cpt.cpt_epoch_advance(ep)
+        start = torch.cuda.Event()
+        start.record(stream)
+        for w in range(P):
+            ws_ = wstreams[w]
+            ws_.wait_event(start)
+            cpt.cpt_grad_scatter(plan, w, dkw[w], [slots_k[o, w] for o in range(P)], slots_k[w, w],
+                                 stream=ws_)
+            cpt.cpt_grad_scatter(plan, w, dvw[w], [slots_v[o, w] for o in range(P)], slots_v[w, w],
+                                 stream=ws_)
+            cpt.cpt_epoch_publish(ep, w, stream=ws_)
+        for o in range(P):
+            os_ = ostreams[o]
+            os_.wait_event(start)
+            cpt.cpt_epoch_wait(ep, o, 1_000_000_000, cpt.CPT_WAIT_BOUNDED, stream=os_)
+            cpt.cpt_slot_reduce(slots_k[o], dko[o], ep.status_ptr(o), stream=os_)
+            cpt.cpt_slot_reduce(slots_v[o], dvo[o], ep.status_ptr(o), stream=os_)
+        for st in wstreams + ostreams:
+            stream.wait_stream(st)
 
     gpu_uuid = None
     try:
@@ -366,17 +410,37 @@ def run_gpu(args):
         host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in part + [dko, dvo]]
         for h, d in zip(host_in, qkv + [dkw, dvw]):
             h.copy_(d)
-        dev_in = qkv + [dkw, dvw]
-        dev_out = part + [dko, dvo]
         h2d = sum(x.numel() * x.element_size() for x in host_in)
         d2h = sum(x.numel() * x.element_size() for x in host_out)
 
+        side = torch.cuda.Stream()
+        h_qkv, h_dkw, h_dvw = host_in[:3], host_in[3], host_in[4]
+        h_part, h_dko, h_dvo = host_out[:3], host_out[3], host_out[4]
+
         def e2e_step():
-            for d, h in zip(dev_in, host_in):
+            # Two independent chains on two streams, so one chain's copies
+            # overlap the other's: Q/K/V in -> plan -> partition -> parts out
+            # on the main stream; dK/dV in -> grad_return (after the plan) ->
+            # owner gradients out on the side stream.
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                dkw.copy_(h_dkw, non_blocking=True)
+                dvw.copy_(h_dvw, non_blocking=True)
+            for d, h in zip(qkv, h_qkv):
                 d.copy_(h, non_blocking=True)
-            step()
-            for h, d in zip(host_out, dev_out):
+            plan = cpt.cpt_plan_create(cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP, P, cu, S, workspace=ws)
+            plan_ready = torch.cuda.Event()
+            plan_ready.record(stream)
+            cpt.cpt_partition(plan, qkv, part)
+            for h, d in zip(h_part, part):
                 h.copy_(d, non_blocking=True)
+            side.wait_event(plan_ready)
+            cpt.cpt_grad_return(plan, dkw, dvw, dko, dvo, stream=side)
+            with torch.cuda.stream(side):
+                h_dko.copy_(dko, non_blocking=True)
+                h_dvo.copy_(dvo, non_blocking=True)
+            stream.wait_stream(side)
+            cpt.cpt_plan_destroy(plan)
 
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
         e2e_step()
@@ -416,7 +480,8 @@ def run_gpu(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded device N(0,1) Q/K/V, N(0,0.02) dK/dV)",
         "config": {"workload": workload(), "P": P, "S": S, "H": H, "D": D,
-                   "layout": "dual_chunk_swap", "parallelism": f"replicas x{world}",
+                   "layout": "dual_chunk_swap", "grad_return_path": PATH,
+                   "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (21.5 GB touched per step), no flush",
                    "step_bytes": step_bytes(S)},
         "grad_return": {"gbs": gr_gbs, "frac_of_peak": gr_gbs / peak, "ms": gr_mean_ms,
@@ -426,7 +491,7 @@ def run_gpu(args):
         "roofline": {"kernel": "grad_return", "bound": "hbm", "achieved": gr_gbs, "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6800 GB/s", "unit": "GB/s", "frac": gr_gbs / peak,
-                     "traffic": profiled_traffic("grad_return", S)},
+                     "traffic": profiled_traffic("grad_return", S) if PATH == "fused" else None},
         "clocks": sampler.summary(t_wall0, t_wall1),
         "gpu_launches": kernels_per_step * args.steps,
         "e2e": e2e,
@@ -527,7 +592,7 @@ def run_slot_reduce_sweep(args):
 
 
 def main():
-    global S, H
+    global S, H, PATH
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -543,12 +608,16 @@ def main():
                     help="target seconds for a whole --impl reference run")
     ap.add_argument("--fixed-sample", action="store_true",
                     help="--impl reference: use --sample-tokens as given")
+    ap.add_argument("--path", choices=["fused", "staged"], default="fused",
+                    help="gradient return as one fused launch (default) or as the staged "
+                         "scatter / publish / wait / reduce flow on 2P streams")
     ap.add_argument("--sweep", choices=["slot_reduce"], default=None,
                     help="instead of the step: the slot-reduce message-size sweep")
     ap.add_argument("--tokens", type=int, default=S, help="S (multiple of 2P)")
     ap.add_argument("--heads", type=int, default=H)
     args = ap.parse_args()
     S, H = args.tokens, args.heads
+    PATH = args.path
     if S % (2 * P) or S <= 0 or H <= 0:
         ap.error("--tokens must be a positive multiple of 8, --heads positive")
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps

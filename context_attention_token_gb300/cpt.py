@@ -157,16 +157,47 @@ def _ptr_array(items):
     return arr
 
 
-def _split(t, parts: int):
-    """A [parts, ...] tensor or a sequence of parts tensors -> list of parts."""
-    if isinstance(t, torch.Tensor):
-        if t.shape[0] != parts:
-            raise ValueError(f"leading dimension {t.shape[0]} != {parts}")
-        return [t[i] for i in range(parts)]
-    t = list(t)
-    if len(t) != parts:
-        raise ValueError(f"expected {parts} tensors, got {len(t)}")
-    return t
+class _Parts:
+    """Device pointers of `parts` equally shaped tensors, given as one
+    contiguous [parts, ...] tensor or as a sequence of tensors, with the
+    shape and dtype of one part."""
+
+    __slots__ = ("ptrs", "shape", "dtype")
+
+    def __init__(self, t, parts: int):
+        if isinstance(t, torch.Tensor):
+            if t.dim() == 0 or t.shape[0] != parts:
+                raise ValueError(f"leading dimension of {tuple(t.shape)} != {parts}")
+            if not t.is_contiguous():
+                raise ValueError("tensors must be contiguous")
+            base = t.data_ptr()
+            step = t.stride(0) * t.element_size()
+            self.ptrs = [base + i * step for i in range(parts)]
+            self.shape = tuple(t.shape[1:])
+            self.dtype = t.dtype
+        else:
+            t = list(t)
+            if len(t) != parts:
+                raise ValueError(f"expected {parts} tensors, got {len(t)}")
+            self.ptrs = [_ptr(x) for x in t]
+            self.shape = tuple(t[0].shape)
+            self.dtype = t[0].dtype
+
+    def array(self):
+        return ctypes.cast((_vp * len(self.ptrs))(*self.ptrs), _vp)
+
+    def row_elems(self) -> int:
+        n = 1
+        for d in self.shape[1:]:
+            n *= int(d)
+        return n
+
+    def code(self) -> int:
+        if self.dtype == torch.float32:
+            return CPT_F32
+        if self.dtype == torch.bfloat16:
+            return CPT_BF16
+        raise TypeError(f"unsupported dtype {self.dtype} (float32 or bfloat16)")
 
 
 def _cu_array(cu_seqlens):
@@ -270,17 +301,14 @@ def cpt_grad_return(plan: Plan, dk_writers, dv_writers, dk_owners, dv_owners, st
     the dV pair may be None.
     """
     P = plan.cp_size
-    dkw = _split(dk_writers, P)
-    dko = _split(dk_owners, P)
-    dvw = _split(dv_writers, P) if dv_writers is not None else None
-    dvo = _split(dv_owners, P) if dv_owners is not None else None
-    row = _row_elems(dkw[0])
+    dkw = _Parts(dk_writers, P)
+    dko = _Parts(dk_owners, P)
+    dvw = _Parts(dv_writers, P) if dv_writers is not None else None
+    dvo = _Parts(dv_owners, P) if dv_owners is not None else None
     _check(_lib.cpt_grad_return(
-        plan.handle, ctypes.cast(_ptr_array(dkw), _vp),
-        ctypes.cast(_ptr_array(dvw), _vp) if dvw is not None else None,
-        ctypes.cast(_ptr_array(dko), _vp),
-        ctypes.cast(_ptr_array(dvo), _vp) if dvo is not None else None,
-        row, _dtype_code(dkw[0]), _dtype_code(dko[0]), _stream(stream)))
+        plan.handle, dkw.array(), dvw.array() if dvw is not None else None, dko.array(),
+        dvo.array() if dvo is not None else None, dkw.row_elems(), dkw.code(), dko.code(),
+        _stream(stream)))
 
 
 CPT_NOALLOC_MAX_TOKENS = 1048576
@@ -295,32 +323,32 @@ def cpt_grad_return_noalloc(layout: int, cp_size: int, cu_seqlens, total_tokens:
     the GPU share that array and race."""
     arr, n = _cu_array(cu_seqlens)
     P = cp_size
-    dkw = _split(dk_writers, P)
-    dko = _split(dk_owners, P)
-    dvw = _split(dv_writers, P) if dv_writers is not None else None
-    dvo = _split(dv_owners, P) if dv_owners is not None else None
+    dkw = _Parts(dk_writers, P)
+    dko = _Parts(dk_owners, P)
+    dvw = _Parts(dv_writers, P) if dv_writers is not None else None
+    dvo = _Parts(dv_owners, P) if dv_owners is not None else None
     _check(_lib.cpt_grad_return_noalloc(
-        layout, P, ctypes.cast(arr, _vp), n, total_tokens, ctypes.cast(_ptr_array(dkw), _vp),
-        ctypes.cast(_ptr_array(dvw), _vp) if dvw is not None else None,
-        ctypes.cast(_ptr_array(dko), _vp),
-        ctypes.cast(_ptr_array(dvo), _vp) if dvo is not None else None,
-        _row_elems(dkw[0]), _dtype_code(dkw[0]), _dtype_code(dko[0]), _stream(stream)))
+        layout, P, ctypes.cast(arr, _vp), n, total_tokens, dkw.array(),
+        dvw.array() if dvw is not None else None, dko.array(),
+        dvo.array() if dvo is not None else None, dkw.row_elems(), dkw.code(), dko.code(),
+        _stream(stream)))
 
 
 def cpt_grad_scatter(plan: Plan, writer: int, src: torch.Tensor, slots, self_slot, stream=None):
     """slots[o] ([T/P, ...]) = writer's rows owned by o; self_slot must be slots[writer]."""
-    P = plan.cp_size
-    sl = _split(slots, P)
-    _check(_lib.cpt_grad_scatter(plan.handle, writer, _ptr(src), ctypes.cast(_ptr_array(sl), _vp),
-                                 _ptr(self_slot), _row_elems(src), _dtype_code(src),
-                                 _stream(stream)))
+    sl = _Parts(slots, plan.cp_size)
+    _check(_lib.cpt_grad_scatter(plan.handle, writer, _ptr(src), sl.array(), _ptr(self_slot),
+                                 _row_elems(src), _dtype_code(src), _stream(stream)))
 
 
 def cpt_slot_reduce(slots, dst: torch.Tensor, status: torch.Tensor | int | None = None, stream=None):
-    sl = list(slots) if not isinstance(slots, torch.Tensor) else [slots[i] for i in range(slots.shape[0])]
-    _check(_lib.cpt_slot_reduce(ctypes.cast(_ptr_array(sl), _vp), len(sl), sl[0].numel(),
-                                _dtype_code(sl[0]), _dtype_code(dst), _ptr(dst), _ptr(status),
-                                _stream(stream)))
+    n = slots.shape[0] if isinstance(slots, torch.Tensor) else len(slots)
+    sl = _Parts(slots, n)
+    numel = 1
+    for d in sl.shape:
+        numel *= int(d)
+    _check(_lib.cpt_slot_reduce(sl.array(), n, numel, sl.code(), _dtype_code(dst), _ptr(dst),
+                                _ptr(status), _stream(stream)))
 
 
 # ------------------------------------------------------------------ epochs
