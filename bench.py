@@ -505,6 +505,96 @@ def run_gpu(args):
     return 0
 
 
+# ---------------------------------------------------------------- next rows
+
+def _median_launch_ms(fn, stream, reps=20, warm=3):
+    import torch
+
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def run_next_rows(args):
+    """One JSON line per widened row, each at the pages' shape unless noted:
+    restore (all-gather inverse reorder), accumulate-into grad_return, the
+    P=2/8 grad_return sweep, the allocation-free grad_return, and a
+    matched-input comparison of the partition policies on the lognormal
+    packed-THD batch (T=131072, 16x128)."""
+    import numpy as np
+    import torch
+
+    from context_attention_token_gb300 import build as cpt_build
+
+    cpt_build.build()
+    from context_attention_token_gb300 import cpt, synth
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    peak, peak_src = load_peak()
+    row = H * D * 2
+
+    def emit(name, ms, nbytes, **extra):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        line = {"next_row": name, "ms": ms, "bytes": nbytes, "gbs": gbs, "frac_of_peak": gbs / peak,
+                "peak": peak, "peak_source": peak_src, **extra}
+        print(json.dumps(line), flush=True)
+
+    # f1: restore K and V from rank-local back to global order
+    plan = cpt.cpt_plan_create(0, P, [0, S], S)
+    kv = [synth.device_normal_bf16((P, S // P, H, D), 6000 + t, 1.0, "cuda") for t in range(2)]
+    back = [torch.empty((S, H, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    ms = _median_launch_ms(lambda: cpt.cpt_restore(plan, kv, back), stream)
+    emit("restore_kv", ms, S * (2 * 2 * row + 2 * 4), tensors=2, S=S, P=P,
+         tok_s=S / (ms / 1e3))
+    del kv, back
+
+    # f4: accumulate-into grad_return, and the P sweep of the plain one
+    for Pw in (2, 4, 8):
+        planp = cpt.cpt_plan_create(0, Pw, [0, S], S)
+        dkw = synth.device_normal_bf16((Pw, S, H, D), 6100 + Pw, 0.02, "cuda")
+        dvw = synth.device_normal_bf16((Pw, S, H, D), 6200 + Pw, 0.02, "cuda")
+        dko = torch.zeros((Pw, S // Pw, H, D), dtype=torch.bfloat16, device="cuda")
+        dvo = torch.zeros_like(dko)
+        ms = _median_launch_ms(lambda: cpt.cpt_grad_return(planp, dkw, dvw, dko, dvo), stream)
+        emit(f"grad_return_P{Pw}", ms, S * (2 * (Pw + 1) * row + 2 * 4), P=Pw, S=S)
+        if Pw == P:
+            ms = _median_launch_ms(
+                lambda: cpt.cpt_grad_return_accumulate(planp, dkw, dvw, dko, dvo), stream)
+            emit("grad_return_accumulate_P4", ms, S * (2 * (Pw + 2) * row + 2 * 4), P=Pw, S=S)
+            ms = _median_launch_ms(
+                lambda: cpt.cpt_grad_return_noalloc(0, Pw, [0, S], S, dkw, dvw, dko, dvo), stream)
+            emit("grad_return_noalloc_P4", ms, S * (2 * (Pw + 1) * row + 2 * 4) + S * 4, P=Pw, S=S,
+                 note="includes its own map build (index-map kernel) each call")
+        del dkw, dvw, dko, dvo
+        torch.cuda.empty_cache()
+
+    # f3 / matched inputs: one lognormal batch (lengths multiples of 8 so all
+    # three policies accept it), Q/K/V [T,16,128]
+    T, Hq = 131072, 16
+    lens = synth.lognormal_doc_lengths(T, synth.rng_for(2, 0), multiple=8)
+    cu = synth.cu_from_lengths(lens)
+    qkv = [synth.device_normal_bf16((T, Hq, D), 6300 + t, 1.0, "cuda") for t in range(3)]
+    out = [torch.empty((P, T // P, Hq, D), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    for name, layout, cuu in (("per_document_dual_chunk_swap", 0, cu),
+                              ("packed_contiguous", 1, cu),
+                              ("mirrored_super_sequence_as_dsc_over_[0,T]", 0, np.array([0, T], np.int32))):
+        pl = cpt.cpt_plan_create(layout, P, cuu, T)
+        ms = _median_launch_ms(lambda: cpt.cpt_partition(pl, qkv, out), stream)
+        emit(f"partition_policy:{name}", ms, T * (3 * 2 * Hq * D * 2 + 3 * 4), T=T, P=P,
+             docs=len(lens), tok_s=T / (ms / 1e3))
+    return 0
+
+
 # ---------------------------------------------------------------- slot-reduce sweep
 
 def run_slot_reduce_sweep(args):
@@ -611,6 +701,9 @@ def main():
     ap.add_argument("--path", choices=["fused", "staged"], default="fused",
                     help="gradient return as one fused launch (default) or as the staged "
                          "scatter / publish / wait / reduce flow on 2P streams")
+    ap.add_argument("--next-rows", action="store_true",
+                    help="instead of the step: restore, accumulate, P sweep, no-alloc and "
+                         "partition-policy lines")
     ap.add_argument("--sweep", choices=["slot_reduce"], default=None,
                     help="instead of the step: the slot-reduce message-size sweep")
     ap.add_argument("--tokens", type=int, default=S, help="S (multiple of 2P)")
@@ -625,6 +718,8 @@ def main():
         return run_reference(args)
     if args.sweep == "slot_reduce":
         return run_slot_reduce_sweep(args)
+    if args.next_rows:
+        return run_next_rows(args)
     return run_gpu(args)
 
 

@@ -44,6 +44,7 @@ CPT_ERR_NOT_PUBLISHED = 10
 
 CPT_LAYOUT_DUAL_CHUNK_SWAP = 0
 CPT_LAYOUT_PACKED_CONTIGUOUS = 1
+CPT_LAYOUT_RETIRED_PACKED_SUPER_SEQUENCE = 2
 CPT_F32 = 0
 CPT_BF16 = 1
 CPT_WAIT_BOUNDED = 0
@@ -75,6 +76,9 @@ _sig("cpt_plan_info", ctypes.c_int, _vp, ctypes.POINTER(_i64), ctypes.POINTER(_i
 _sig("cpt_index_map", ctypes.c_int, _vp, _vp, _vp, _vp)
 _sig("cpt_thd_metadata", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("cpt_partition", ctypes.c_int, _vp, _i32, _vp, _vp, _i64, ctypes.c_int, _vp)
+_sig("cpt_grad_return_accumulate", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, ctypes.c_int,
+     ctypes.c_int, _vp)
+_sig("cpt_restore", ctypes.c_int, _vp, _i32, _vp, _vp, _i64, ctypes.c_int, _vp)
 _sig("cpt_grad_return", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, ctypes.c_int, ctypes.c_int, _vp)
 _sig("cpt_grad_return_noalloc", ctypes.c_int, ctypes.c_int, _i32, _vp, _i32, _i64, _vp, _vp, _vp, _vp,
      _i64, ctypes.c_int, ctypes.c_int, _vp)
@@ -286,6 +290,16 @@ def cpt_partition(plan: Plan, srcs, dsts, stream=None):
                               _stream(stream)))
 
 
+def cpt_restore(plan: Plan, srcs, dsts, stream=None):
+    """dsts[t] ([T, ...]) = global-order copy of the rank-local srcs[t] ([P, T/P, ...])."""
+    srcs, dsts = list(srcs), list(dsts)
+    if len(srcs) != len(dsts):
+        raise ValueError("srcs and dsts differ in length")
+    _check(_lib.cpt_restore(plan.handle, len(srcs), ctypes.cast(_ptr_array(srcs), _vp),
+                            ctypes.cast(_ptr_array(dsts), _vp), _row_elems(dsts[0]),
+                            _dtype_code(srcs[0]), _stream(stream)))
+
+
 def _row_elems(t: torch.Tensor) -> int:
     """Elements of one token row of a [T, ...] tensor."""
     n = 1
@@ -294,21 +308,31 @@ def _row_elems(t: torch.Tensor) -> int:
     return n
 
 
+def _grad_return(fn, plan: Plan, dk_writers, dv_writers, dk_owners, dv_owners, stream):
+    P = plan.cp_size
+    dkw = _Parts(dk_writers, P)
+    dko = _Parts(dk_owners, P)
+    dvw = _Parts(dv_writers, P) if dv_writers is not None else None
+    dvo = _Parts(dv_owners, P) if dv_owners is not None else None
+    _check(fn(plan.handle, dkw.array(), dvw.array() if dvw is not None else None, dko.array(),
+              dvo.array() if dvo is not None else None, dkw.row_elems(), dkw.code(), dko.code(),
+              _stream(stream)))
+
+
 def cpt_grad_return(plan: Plan, dk_writers, dv_writers, dk_owners, dv_owners, stream=None):
     """Owners' local dK (and dV) = ordered sum over writers' global gradients.
 
     Each of the four arguments is a [P, ...] tensor or a list of P tensors;
     the dV pair may be None.
     """
-    P = plan.cp_size
-    dkw = _Parts(dk_writers, P)
-    dko = _Parts(dk_owners, P)
-    dvw = _Parts(dv_writers, P) if dv_writers is not None else None
-    dvo = _Parts(dv_owners, P) if dv_owners is not None else None
-    _check(_lib.cpt_grad_return(
-        plan.handle, dkw.array(), dvw.array() if dvw is not None else None, dko.array(),
-        dvo.array() if dvo is not None else None, dkw.row_elems(), dkw.code(), dko.code(),
-        _stream(stream)))
+    _grad_return(_lib.cpt_grad_return, plan, dk_writers, dv_writers, dk_owners, dv_owners, stream)
+
+
+def cpt_grad_return_accumulate(plan: Plan, dk_writers, dv_writers, dk_owners, dv_owners,
+                               stream=None):
+    """As cpt_grad_return, but the owners' current values start the sums."""
+    _grad_return(_lib.cpt_grad_return_accumulate, plan, dk_writers, dv_writers, dk_owners,
+                 dv_owners, stream)
 
 
 CPT_NOALLOC_MAX_TOKENS = 1048576

@@ -164,6 +164,11 @@ WsLayout ws_layout(int P, int n, int64_t T)
 
 cpt_status check_sizes(cpt_layout layout, int32_t P, int32_t n, int64_t T)
 {
+    if ((int)layout == CPT_LAYOUT_RETIRED_PACKED_SUPER_SEQUENCE)
+        return fail(CPT_ERR_UNSUPPORTED,
+                    "layout %d is the retired mirrored packed_super_sequence policy; use "
+                    "PACKED_CONTIGUOUS, or a DUAL_CHUNK_SWAP plan over cu_seqlens = {0, T} for "
+                    "its map", (int)layout);
     if (layout != CPT_LAYOUT_DUAL_CHUNK_SWAP && layout != CPT_LAYOUT_PACKED_CONTIGUOUS)
         return fail(CPT_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
     if (P < 1 || P > CPT_MAX_CP_SIZE)
@@ -457,9 +462,51 @@ cpt_status cpt_partition(const cpt_plan *plan, int32_t n_tensors, const void *co
     return e == cudaSuccess ? CPT_OK : cuda_fail(e, "partition launch");
 }
 
-cpt_status cpt_grad_return(const cpt_plan *plan, const void *const *dkw, const void *const *dvw,
-                           void *const *dko, void *const *dvo, int64_t row_elems, cpt_dtype in,
-                           cpt_dtype out, void *stream)
+cpt_status cpt_restore(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
+                       void *const *dst, int64_t row_elems, cpt_dtype dtype, void *stream)
+{
+    int dev = 0;
+    cpt_status st = check_plan(plan, &dev);
+    if (st) return st;
+    if (n_tensors < 1 || n_tensors > kMaxTensors)
+        return fail(CPT_ERR_INVALID_ARG, "n_tensors %d outside 1..3", n_tensors);
+    if (src == nullptr || dst == nullptr) return fail(CPT_ERR_INVALID_ARG, "src or dst is NULL");
+    int64_t units = 0;
+    if ((st = check_row(row_elems, dtype, dtype, &units))) return st;
+    if (plan->T == 0) return CPT_OK;
+    const int64_t row_bytes = units * 16;
+    std::vector<Range> r;
+    add_range(r, plan->ws, plan->ws_bytes, false, "workspace");
+    for (int t = 0; t < n_tensors; ++t) {
+        if ((st = check_ptr(src[t], dev, 16, "src", t))) return st;
+        if ((st = check_ptr(dst[t], dev, 16, "dst", t))) return st;
+        add_range(r, src[t], (size_t)(plan->T * row_bytes), false, "src", t);
+        add_range(r, dst[t], (size_t)(plan->T * row_bytes), true, "dst", t);
+    }
+    if ((st = check_overlaps(r))) return st;
+
+    // global row g of piece r (g = r*T/P + j) reads local row g2l[g]
+    GatherParams p;
+    memset(&p, 0, sizeof p);
+    p.l2g = plan->layout == CPT_LAYOUT_PACKED_CONTIGUOUS ? nullptr : plan->g2l;
+    for (int t = 0; t < n_tensors; ++t) {
+        p.src[t] = static_cast<const uint8_t *>(src[t]);
+        for (int o = 0; o < plan->P; ++o)
+            p.dst[t][o] = static_cast<uint8_t *>(dst[t]) + (int64_t)o * plan->Tp * row_bytes;
+    }
+    p.T = plan->T;
+    p.Tp = plan->Tp;
+    p.rows = (int64_t)n_tensors * plan->T;
+    p.units = (int32_t)units;
+    p.row_bytes = (int32_t)row_bytes;
+    cudaError_t e = launch_gather(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CPT_OK : cuda_fail(e, "restore launch");
+}
+
+static cpt_status grad_return_impl(const cpt_plan *plan, const void *const *dkw,
+                                   const void *const *dvw, void *const *dko, void *const *dvo,
+                                   int64_t row_elems, cpt_dtype in, cpt_dtype out, void *stream,
+                                   bool accumulate)
 {
     int dev = 0;
     cpt_status st = check_plan(plan, &dev);
@@ -504,8 +551,23 @@ cpt_status cpt_grad_return(const cpt_plan *plan, const void *const *dkw, const v
     p.units = (int32_t)units;
     p.in_row_bytes = (int32_t)in_row;
     p.out_row_bytes = (int32_t)out_row;
-    cudaError_t e = launch_grad_return(p, P, in, out, static_cast<cudaStream_t>(stream));
+    cudaError_t e =
+        launch_grad_return(p, P, in, out, static_cast<cudaStream_t>(stream), accumulate);
     return e == cudaSuccess ? CPT_OK : cuda_fail(e, "grad_return launch");
+}
+
+cpt_status cpt_grad_return(const cpt_plan *plan, const void *const *dkw, const void *const *dvw,
+                           void *const *dko, void *const *dvo, int64_t row_elems, cpt_dtype in,
+                           cpt_dtype out, void *stream)
+{
+    return grad_return_impl(plan, dkw, dvw, dko, dvo, row_elems, in, out, stream, false);
+}
+
+cpt_status cpt_grad_return_accumulate(const cpt_plan *plan, const void *const *dkw,
+                                      const void *const *dvw, void *const *dko, void *const *dvo,
+                                      int64_t row_elems, cpt_dtype in, cpt_dtype out, void *stream)
+{
+    return grad_return_impl(plan, dkw, dvw, dko, dvo, row_elems, in, out, stream, true);
 }
 
 cpt_status cpt_grad_scatter(const cpt_plan *plan, int32_t writer, const void *src,

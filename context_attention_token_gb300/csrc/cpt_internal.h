@@ -42,7 +42,8 @@ struct GatherParams {
 };
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream);
 
-// a5: fused owner-gradient return for one or two tensors (dK, dV).
+// a5: fused owner-gradient return for one or two tensors (dK, dV); with
+// `accumulate` the owners' current values start the sums.
 struct GradReturnParams {
     const int32_t *l2g;              // [T]
     const uint8_t *w[2][kMaxCp];     // writer w's global gradient [T][in_row_bytes]
@@ -55,7 +56,7 @@ struct GradReturnParams {
     int32_t out_row_bytes;
 };
 cudaError_t launch_grad_return(const GradReturnParams &p, int cp_size, int in_dtype,
-                               int out_dtype, cudaStream_t stream);
+                               int out_dtype, cudaStream_t stream, bool accumulate = false);
 
 // a7: dst[i] = ordered binary32 sum of slot_0..slot_{n-1}[i].
 struct SlotReduceParams {

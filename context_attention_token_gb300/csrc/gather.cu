@@ -1,14 +1,16 @@
-// Row gather into rank-local order: the Q/K/V reorder of "[PyTorch] Add
-// experimental packed-contiguous THD all-gather CP" (TransformerEngine PR
-// 3221, commit "Reuse the existing THD CUDA partition and reorder kernels
-// ...") and the per-writer scatter into owner slots of "Add stream-ordered CP
-// gradient return primitive" (TransformerEngine PR 3235, sequence diagram).
+// Row gather between global and rank-local token order, used three ways:
+//  - the Q/K/V reorder of "[PyTorch] Add experimental packed-contiguous THD
+//    all-gather CP" (TransformerEngine PR 3221, commit "Reuse the existing THD
+//    CUDA partition and reorder kernels ..."): index = l2g;
+//  - its inverse after an all-gather, back to global order: index = g2l;
+//  - the per-writer scatter into owner slots of "Add stream-ordered CP
+//    gradient return primitive" (TransformerEngine PR 3235, sequence diagram):
+//    index = l2g, one destination pointer per owner.
 //
 // HBM-bound bit copy: every output row is one source row. A warp owns one row
 // at a time and moves it in 16-byte units, kUnroll units per lane in flight
-// before the first store, so a full SM keeps ~kUnroll * 16 B * 2048 threads of
-// loads outstanding. Rows are visited in output order by a grid-stride loop,
-// so concurrently active warps read and write neighbouring rows.
+// before the first store. Rows are visited in output order by a grid-stride
+// loop, so concurrently active warps read and write neighbouring rows.
 #include "cpt_device.cuh"
 #include "cpt_internal.h"
 

@@ -67,7 +67,33 @@ __device__ __forceinline__ void store_unit(uint8_t *p, const float (&a)[E])
     }
 }
 
-template <int P, int IN, int OUT, int U>
+// Widen the current owner values of one unit (ACC mode). A coherent
+// streaming load: this thread overwrites the same bytes afterwards.
+template <int OUT, int E>
+__device__ __forceinline__ void load_unit(const uint8_t *p, float (&a)[E])
+{
+    if constexpr (OUT == kBf16) {
+        if constexpr (E == 8) {
+            const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p));
+            a[0] = bf16_lo(v.x); a[1] = bf16_hi(v.x); a[2] = bf16_lo(v.y); a[3] = bf16_hi(v.y);
+            a[4] = bf16_lo(v.z); a[5] = bf16_hi(v.z); a[6] = bf16_lo(v.w); a[7] = bf16_hi(v.w);
+        } else {
+            const uint2 v = __ldcs(reinterpret_cast<const uint2 *>(p));
+            a[0] = bf16_lo(v.x); a[1] = bf16_hi(v.x); a[2] = bf16_lo(v.y); a[3] = bf16_hi(v.y);
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < E; h += 4) {
+            const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p + h * 4));
+            a[h] = __uint_as_float(v.x); a[h + 1] = __uint_as_float(v.y);
+            a[h + 2] = __uint_as_float(v.z); a[h + 3] = __uint_as_float(v.w);
+        }
+    }
+}
+
+// ACC = false: out = round(x_0 + x_1 + ... + x_{P-1}), accumulator from x_0.
+// ACC = true:  out = round(out + x_0 + ... + x_{P-1}), accumulator from out.
+template <int P, int IN, int OUT, int U, bool ACC>
 __global__ void __launch_bounds__(kThreads) grad_return_kernel(const GradReturnParams p)
 {
     constexpr int E = Unit<IN>::kElems;
@@ -102,27 +128,32 @@ __global__ void __launch_bounds__(kThreads) grad_return_kernel(const GradReturnP
             for (int k = 0; k < U; ++k) {
                 const int u = u0 + 32 * k;
                 if (u < units) {
+                    uint8_t *out = dst + (int64_t)u * kOutUnitBytes;
                     float acc[E];
-                    Unit<IN>::widen(v[k][0], acc);
+                    if constexpr (ACC) {
+                        load_unit<OUT>(out, acc);
+                    } else {
+                        Unit<IN>::widen(v[k][0], acc);
+                    }
 #pragma unroll
-                    for (int w = 1; w < P; ++w) {
+                    for (int w = ACC ? 0 : 1; w < P; ++w) {
                         float x[E];
                         Unit<IN>::widen(v[k][w], x);
 #pragma unroll
                         for (int e = 0; e < E; ++e) acc[e] = add_rn(acc[e], x[e]);
                     }
-                    store_unit<OUT>(dst + (int64_t)u * kOutUnitBytes, acc);
+                    store_unit<OUT>(out, acc);
                 }
             }
         }
     }
 }
 
-template <int P, int IN, int OUT>
+template <int P, int IN, int OUT, bool ACC>
 cudaError_t launch_typed(const GradReturnParams &p, cudaStream_t stream)
 {
     constexpr int U = P <= 4 ? 2 : 1;
-    auto kernel = grad_return_kernel<P, IN, OUT, U>;
+    auto kernel = grad_return_kernel<P, IN, OUT, U, ACC>;
     static int blocks_per_sm[64] = {0};  // per device, one table per instantiation
     int dev = 0;
     cudaGetDevice(&dev);
@@ -140,32 +171,39 @@ cudaError_t launch_typed(const GradReturnParams &p, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template <int P>
+template <int P, bool ACC>
 cudaError_t launch_p(const GradReturnParams &p, int in, int out, cudaStream_t s)
 {
-    if (in == kBf16 && out == kBf16) return launch_typed<P, kBf16, kBf16>(p, s);
-    if (in == kBf16 && out == kF32) return launch_typed<P, kBf16, kF32>(p, s);
-    if (in == kF32 && out == kBf16) return launch_typed<P, kF32, kBf16>(p, s);
-    return launch_typed<P, kF32, kF32>(p, s);
+    if (in == kBf16 && out == kBf16) return launch_typed<P, kBf16, kBf16, ACC>(p, s);
+    if (in == kBf16 && out == kF32) return launch_typed<P, kBf16, kF32, ACC>(p, s);
+    if (in == kF32 && out == kBf16) return launch_typed<P, kF32, kBf16, ACC>(p, s);
+    return launch_typed<P, kF32, kF32, ACC>(p, s);
+}
+
+template <bool ACC>
+cudaError_t launch_acc(const GradReturnParams &p, int cp_size, int in, int out, cudaStream_t s)
+{
+    switch (cp_size) {
+    case 1: return launch_p<1, ACC>(p, in, out, s);
+    case 2: return launch_p<2, ACC>(p, in, out, s);
+    case 3: return launch_p<3, ACC>(p, in, out, s);
+    case 4: return launch_p<4, ACC>(p, in, out, s);
+    case 5: return launch_p<5, ACC>(p, in, out, s);
+    case 6: return launch_p<6, ACC>(p, in, out, s);
+    case 7: return launch_p<7, ACC>(p, in, out, s);
+    case 8: return launch_p<8, ACC>(p, in, out, s);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_grad_return(const GradReturnParams &p, int cp_size, int in_dtype,
-                               int out_dtype, cudaStream_t stream)
+                               int out_dtype, cudaStream_t stream, bool accumulate)
 {
     if (p.rows == 0) return cudaSuccess;
-    switch (cp_size) {
-    case 1: return launch_p<1>(p, in_dtype, out_dtype, stream);
-    case 2: return launch_p<2>(p, in_dtype, out_dtype, stream);
-    case 3: return launch_p<3>(p, in_dtype, out_dtype, stream);
-    case 4: return launch_p<4>(p, in_dtype, out_dtype, stream);
-    case 5: return launch_p<5>(p, in_dtype, out_dtype, stream);
-    case 6: return launch_p<6>(p, in_dtype, out_dtype, stream);
-    case 7: return launch_p<7>(p, in_dtype, out_dtype, stream);
-    case 8: return launch_p<8>(p, in_dtype, out_dtype, stream);
-    default: return cudaErrorInvalidValue;
-    }
+    return accumulate ? launch_acc<true>(p, cp_size, in_dtype, out_dtype, stream)
+                      : launch_acc<false>(p, cp_size, in_dtype, out_dtype, stream);
 }
 
 }  // namespace cpt

@@ -93,6 +93,15 @@ typedef enum cpt_layout {
     CPT_LAYOUT_PACKED_CONTIGUOUS = 1
 } cpt_layout;
 
+/* The mirrored "packed_super_sequence" policy (2P chunks over the whole
+ * packed buffer, rank r owning chunks r and 2P-1-r) was retired in favour of
+ * PACKED_CONTIGUOUS as the only packed opt-in ([TE-3221] commit "Keep
+ * per-document partitioning as the default ...", which keeps a negative test
+ * for the retired selector). Passing this value is rejected with
+ * CPT_ERR_UNSUPPORTED. Its ownership map is exactly a DUAL_CHUNK_SWAP plan
+ * over cu_seqlens = {0, T}, which stays available for comparisons. */
+#define CPT_LAYOUT_RETIRED_PACKED_SUPER_SEQUENCE 2
+
 /* Element types. Sums are always accumulated in binary32. */
 typedef enum cpt_dtype { CPT_F32 = 0, CPT_BF16 = 1 } cpt_dtype;
 
@@ -235,6 +244,19 @@ CPT_API cpt_status cpt_thd_metadata(const cpt_plan *plan, int32_t *num_segs, int
 CPT_API cpt_status cpt_partition(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
                          void *const *dst, int64_t row_elems, cpt_dtype dtype, void *stream);
 
+/* All-gather restore: put rank-local token tensors back into global order,
+ * the inverse of cpt_partition ([TE-3221] "Scope and constraints": all-gather
+ * CP; commit "Allow relaxed THD all-gather ...": rank-major ownership is the
+ * policy that needs no KV reorder, so the per-document one does):
+ *   dst[t][g] = src[t][g2l[g]], i.e. dst[t][l2g[q]] = src[t][q], a bit copy.
+ *  src        host array of n_tensors device pointers, each [P][T/P][row]
+ *             (the all-gathered rank-major buffer).
+ *  dst        host array of n_tensors device pointers, each [T][row]; must
+ *             not overlap any src or another dst.
+ *  Other arguments and errors: as cpt_partition. */
+CPT_API cpt_status cpt_restore(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
+                               void *const *dst, int64_t row_elems, cpt_dtype dtype, void *stream);
+
 /* ------------------------------------------------------------------ */
 /* Fused owner-gradient return                                         */
 /* ------------------------------------------------------------------ */
@@ -259,6 +281,19 @@ CPT_API cpt_status cpt_grad_return(const cpt_plan *plan, const void *const *dk_w
                            const void *const *dv_writers, void *const *dk_owners,
                            void *const *dv_owners, int64_t row_elems, cpt_dtype in,
                            cpt_dtype out, void *stream);
+
+/* As cpt_grad_return, but the owners' current gradients start the sums (the
+ * other reading of "accumulates four writer slots into the local owner's
+ * dK/dV", [TE-3235] "Description"):
+ *   out[o][j] = round((((out[o][j] + x_0) + x_1) + ...) + x_{P-1}),
+ * the existing owner value widened exactly to binary32 first. Each owner row
+ * is read once more than in cpt_grad_return. Arguments and errors: as
+ * cpt_grad_return. */
+CPT_API cpt_status cpt_grad_return_accumulate(const cpt_plan *plan, const void *const *dk_writers,
+                                              const void *const *dv_writers,
+                                              void *const *dk_owners, void *const *dv_owners,
+                                              int64_t row_elems, cpt_dtype in, cpt_dtype out,
+                                              void *stream);
 
 /* Largest batch cpt_grad_return_noalloc accepts. */
 #define CPT_NOALLOC_MAX_TOKENS 1048576

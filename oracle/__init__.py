@@ -74,6 +74,8 @@ def _load():
             lib.oracle_thd_metadata.restype = ctypes.c_int
             lib.oracle_partition.argtypes = [i32p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
             lib.oracle_partition.restype = None
+            lib.oracle_restore.argtypes = [i32p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+            lib.oracle_restore.restype = None
             lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
             lib.oracle_bf16_to_f32.restype = ctypes.c_float
             lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -84,6 +86,10 @@ def _load():
             lib.oracle_grad_return.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                                ctypes.c_int, i32p, ctypes.c_void_p, ctypes.c_void_p]
             lib.oracle_grad_return.restype = None
+            lib.oracle_grad_return_accumulate.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                                          ctypes.c_int, ctypes.c_int, i32p, ctypes.c_void_p,
+                                                          ctypes.c_void_p]
+            lib.oracle_grad_return_accumulate.restype = None
             lib.oracle_grad_scatter.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, i32p,
                                                 ctypes.c_void_p, ctypes.c_void_p]
             lib.oracle_grad_scatter.restype = None
@@ -160,6 +166,17 @@ def partition(l2g: np.ndarray, src: np.ndarray) -> np.ndarray:
     return dst
 
 
+def restore(l2g: np.ndarray, local: np.ndarray) -> np.ndarray:
+    """global[l2g[q]] = local[q] for a flattened rank-major [T, ...] array."""
+    local = np.ascontiguousarray(local)
+    l2g = np.ascontiguousarray(l2g, dtype=np.int32)
+    T = local.shape[0]
+    out = np.empty_like(local)
+    row_bytes = local.nbytes // T if T else 0
+    _load().oracle_restore(_ptr(l2g), T, _ptr(local), _ptr(out), row_bytes)
+    return out
+
+
 def f32_to_bf16(x: float) -> int:
     return int(_load().oracle_f32_to_bf16(float(x)))
 
@@ -204,6 +221,22 @@ def grad_return(l2g: np.ndarray, writers, out_dtype: int):
     _load().oracle_grad_return(P, T, row_elems, in_code, out_dtype, _ptr(l2g),
                                ctypes.cast(warr, ctypes.c_void_p), ctypes.cast(oarr, ctypes.c_void_p))
     return owners
+
+
+def grad_return_accumulate(l2g: np.ndarray, writers, owners):
+    """New owner arrays: each owner's current values plus the ordered writer sum."""
+    writers = [np.ascontiguousarray(w) for w in writers]
+    P = len(writers)
+    T = writers[0].shape[0]
+    row_elems = writers[0].size // T if T else 0
+    out = [np.array(o, copy=True, order="C") for o in owners]
+    l2g = np.ascontiguousarray(l2g, dtype=np.int32)
+    warr = (ctypes.c_void_p * P)(*[_ptr(w) for w in writers])
+    oarr = (ctypes.c_void_p * P)(*[_ptr(o) for o in out])
+    _load().oracle_grad_return_accumulate(P, T, row_elems, _dtype_code(writers[0]), _dtype_code(out[0]),
+                                          _ptr(l2g), ctypes.cast(warr, ctypes.c_void_p),
+                                          ctypes.cast(oarr, ctypes.c_void_p))
+    return out
 
 
 def grad_scatter(l2g: np.ndarray, writer: np.ndarray, cp_size: int):

@@ -188,6 +188,24 @@ void oracle_partition(const int32_t *l2g, int64_t T, const void *src, void *dst,
 }
 
 /* ------------------------------------------------------------------ */
+/* All-gather restore: the inverse of the reorder. After an all-gather */
+/* every rank holds the rank-major buffer [P][T/P][row]; the per-      */
+/* document layout must be put back into global token order before    */
+/* attention sees it ([TE-3221] commit "Allow relaxed THD all-gather   */
+/* ...": rank-major ownership is the case that needs no KV reorder).   */
+/* Written as the definition: local row q goes to global row l2g[q].   */
+/* Parity: pinned (round trip with the partition, brute-force map).    */
+/* ------------------------------------------------------------------ */
+void oracle_restore(const int32_t *l2g, int64_t T, const void *local, void *global,
+                    int64_t row_bytes)
+{
+    const uint8_t *s = (const uint8_t *)local;
+    uint8_t *d = (uint8_t *)global;
+    for (int64_t q = 0; q < T; ++q)
+        memcpy(d + (int64_t)l2g[q] * row_bytes, s + q * row_bytes, (size_t)row_bytes);
+}
+
+/* ------------------------------------------------------------------ */
 /* bf16 <-> f32.                                                       */
 /* bf16 is the top half of a binary32 word, so widening is exact.      */
 /* Narrowing rounds to nearest, ties to even, from the bit definition: */
@@ -272,6 +290,33 @@ void oracle_grad_return(int P, int64_t T, int64_t row_elems, int in_dtype, int o
             for (int64_t e = 0; e < row_elems; ++e) {
                 float acc = load_elem(writers[0], in_dtype, g * row_elems + e);
                 for (int w = 1; w < P; ++w)
+                    acc = acc + load_elem(writers[w], in_dtype, g * row_elems + e);
+                store_elem(owners[o], out_dtype, j * row_elems + e, acc);
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Owner-gradient return that adds into the owner's existing gradient  */
+/* (the other reading of "accumulates four writer slots into the local */
+/* owner's dK/dV", [TE-3235] "Description"): the accumulator starts    */
+/* from the owner's current value, then adds writers 0..P-1 in order:  */
+/*   out = round(((out + x_0) + x_1) + ... + x_{P-1}).                 */
+/* Parity: pinned (ones into ones, order canary with a start value,    */
+/* numpy binary32 adds).                                               */
+/* ------------------------------------------------------------------ */
+void oracle_grad_return_accumulate(int P, int64_t T, int64_t row_elems, int in_dtype,
+                                   int out_dtype, const int32_t *l2g, const void *const *writers,
+                                   void *const *owners)
+{
+    int64_t Tp = T / P;
+    for (int o = 0; o < P; ++o) {
+        for (int64_t j = 0; j < Tp; ++j) {
+            int64_t g = l2g[(int64_t)o * Tp + j];
+            for (int64_t e = 0; e < row_elems; ++e) {
+                float acc = load_elem(owners[o], out_dtype, j * row_elems + e);
+                for (int w = 0; w < P; ++w)
                     acc = acc + load_elem(writers[w], in_dtype, g * row_elems + e);
                 store_elem(owners[o], out_dtype, j * row_elems + e, acc);
             }

@@ -73,7 +73,7 @@ def test_validate_layout_agrees_with_oracle(cpt, oracle_lib, layout):
 def test_validate_layout_rejects_bad_arguments(cpt):
     assert cpt.cpt_validate_layout(0, 0, [0, 8], 8) == cpt.CPT_ERR_INVALID_ARG
     assert cpt.cpt_validate_layout(0, 9, [0, 18], 18) == cpt.CPT_ERR_INVALID_ARG
-    assert cpt.cpt_validate_layout(2, 2, [0, 8], 8) == cpt.CPT_ERR_INVALID_ARG
+    assert cpt.cpt_validate_layout(3, 2, [0, 8], 8) == cpt.CPT_ERR_INVALID_ARG
     assert cpt.cpt_validate_layout(0, 2, [0, 6], 6) == cpt.CPT_ERR_NOT_DIVISIBLE
     assert "not a multiple" in cpt.cpt_last_error_string()
     assert cpt.cpt_validate_layout(1, 4, [0, 6], 6) == cpt.CPT_ERR_NOT_DIVISIBLE
@@ -88,3 +88,29 @@ def test_workspace_bytes(cpt):
     assert cpt.cpt_plan_workspace_bytes(0, 4, 100, 262144) > a
     assert cpt.cpt_plan_workspace_bytes(0, 9, 1, 64) == 0
     assert cpt.cpt_plan_workspace_bytes(0, 2, 1, 1 << 31) == 0
+
+
+def test_retired_packed_super_sequence_selector_is_rejected(cpt):
+    """The mirrored packed_super_sequence policy was retired; its selector
+    must fail closed, on the host, with a message that says so."""
+    code = cpt.CPT_LAYOUT_RETIRED_PACKED_SUPER_SEQUENCE
+    assert cpt.cpt_validate_layout(code, 4, [0, 64], 64) == cpt.CPT_ERR_UNSUPPORTED
+    assert "retired" in cpt.cpt_last_error_string()
+    assert cpt.cpt_plan_workspace_bytes(code, 4, 1, 64) == 0
+    assert cpt.cpt_validate_layout(3, 4, [0, 64], 64) == cpt.CPT_ERR_INVALID_ARG
+
+
+def test_mirrored_map_is_dsc_over_one_sequence(oracle_lib):
+    """2P mirrored chunks over the whole buffer = a per-document plan over
+    cu_seqlens [0, T]: rank r holds chunks r and 2P-1-r of the buffer."""
+    import numpy as np
+
+    o = oracle_lib
+    for P in (2, 4, 8):
+        T = 2 * P * 7
+        l2g, _ = o.index_map(o.LAYOUT_DSC, P, [0, T], T)
+        m = T // (2 * P)
+        for r in range(P):
+            want = list(range(r * m, (r + 1) * m)) + list(range((2 * P - 1 - r) * m, (2 * P - r) * m))
+            assert l2g[r * 2 * m:(r + 1) * 2 * m].tolist() == want
+        assert np.array_equal(np.sort(l2g), np.arange(T))

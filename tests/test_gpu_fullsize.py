@@ -112,5 +112,11 @@ def test_partition_pages_shape_sampled(cpt, big_plan):
     gi = torch.from_numpy(l2g.astype(np.int64)).cuda()
     for x, d in zip(qkv, dst):
         assert torch.equal(d.view(S, H, D).view(torch.int16), x.index_select(0, gi).view(torch.int16))
-    del qkv, dst
+    # all-gather restore of K and V gives back the inputs bit for bit
+    back = [torch.empty((S, H, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    cpt.cpt_restore(plan, dst[1:], back)
+    torch.cuda.synchronize()
+    for x, b in zip(qkv[1:], back):
+        assert torch.equal(b.view(torch.int16), x.view(torch.int16))
+    del qkv, dst, back
     torch.cuda.empty_cache()

@@ -134,6 +134,31 @@ def test_partition_matches_oracle(cpt, cuda_device, layout, P, lens, row_shape, 
         assert d.bands_intact()
 
 
+@pytest.mark.parametrize("layout,P,lens,row_shape,dt", [
+    (DSC, 2, [16, 24, 24], (2, 8), "f32"),
+    (PACKED, 2, [16, 24, 24], (2, 8), "f32"),
+    (DSC, 4, [8 * 3, 8 * 500, 0, 8 * 211], (3, 40), "bf16"),
+    (PACKED, 3, [7, 1000, 3, 2590], (8, 16), "bf16"),
+    (DSC, 8, [16 * 64, 16 * 3], (20, 128), "bf16"),
+    (DSC, 1, [10, 0, 22], (1, 4), "f32"),
+])
+def test_restore_matches_oracle(cpt, cuda_device, layout, P, lens, row_shape, dt):
+    """All-gather restore: rank-local [P, T/P, ...] back to global order."""
+    cu = _cu(lens)
+    T = int(cu[-1])
+    rng = np.random.default_rng(17)
+    locs = [_rand_rows(rng, T, row_shape, dt) for _ in range(3)]
+    plan = cpt.cpt_plan_create(layout, P, cu, T)
+    src = [to_dev(x).view((P, T // P) + row_shape) for x in locs]
+    dst = [Guarded((T,) + row_shape, src[0].dtype) for _ in range(3)]
+    cpt.cpt_restore(plan, src, [d.t for d in dst])
+    torch.cuda.synchronize()
+    l2g, _ = oracle.index_map(layout, P, cu, T)
+    for x, d in zip(locs, dst):
+        assert np.array_equal(bits(to_host(d.t)), bits(oracle.restore(l2g, x)))
+        assert d.bands_intact()
+
+
 def test_partition_row_ids(cpt, cuda_device):
     """Rows carry their global id in every 16-bit word: the output shows the map."""
     P, cu = 4, _cu([8 * 11, 8 * 40, 8 * 5])
@@ -249,6 +274,46 @@ def test_grad_return_single_doc_config(cpt, cuda_device):
             for v in vals[1:]:
                 acc = np.add(acc, v, dtype=np.float32)
             assert np.array_equal(h[r][j], oracle.f32_to_bf16_array(acc))
+
+
+@pytest.mark.parametrize("case", GR_CASES, ids=lambda c: f"L{c[0]}P{c[1]}{c[4]}to{c[5]}")
+def test_grad_return_accumulate_matches_oracle(cpt, cuda_device, case):
+    """Accumulate-into mode: the owners' current values start the ordered sums."""
+    layout, P, lens, row_shape, din, dout = case
+    cu = _cu(lens)
+    T = int(cu[-1])
+    rng = np.random.default_rng(3000 + P)
+    wk = _writers(rng, P, T, row_shape, din)
+    wv = _writers(rng, P, T, row_shape, din)
+    if dout == "f32":
+        sk = [synth.uniform_f32(rng, (T // P,) + row_shape, -3, 3) for _ in range(P)]
+        sv = [synth.uniform_f32(rng, (T // P,) + row_shape, -3, 3) for _ in range(P)]
+    else:
+        sk = [synth.uniform_bf16(rng, (T // P,) + row_shape, -3, 3) for _ in range(P)]
+        sv = [synth.uniform_bf16(rng, (T // P,) + row_shape, -3, 3) for _ in range(P)]
+    plan = cpt.cpt_plan_create(layout, P, cu, T)
+    ok = [to_dev(x) for x in sk]
+    ov = [to_dev(x) for x in sv]
+    cpt.cpt_grad_return_accumulate(plan, [to_dev(w) for w in wk], [to_dev(w) for w in wv], ok, ov)
+    torch.cuda.synchronize()
+    l2g, _ = oracle.index_map(layout, P, cu, T)
+    for ws, starts, outs in ((wk, sk, ok), (wv, sv, ov)):
+        want = oracle.grad_return_accumulate(l2g, ws, starts)
+        for o in range(P):
+            assert np.array_equal(bits(to_host(outs[o])), bits(want[o])), f"owner {o}"
+
+
+@pytest.mark.parametrize("P", [2, 4, 8])
+def test_grad_return_accumulate_closed_forms(cpt, cuda_device, P):
+    cu = _cu([2 * P * 64])
+    T = int(cu[-1])
+    plan = cpt.cpt_plan_create(DSC, P, cu, T)
+    w = torch.ones((P, T, 64), dtype=torch.bfloat16, device="cuda")
+    o = torch.ones((P, T // P, 64), dtype=torch.bfloat16, device="cuda")
+    cpt.cpt_grad_return_accumulate(plan, w, None, o, None)
+    cpt.cpt_grad_return_accumulate(plan, w, None, o, None)
+    torch.cuda.synchronize()
+    assert bool((o == 2 * P + 1).all().item())
 
 
 @pytest.mark.parametrize("P", [1, 2, 3, 4, 8])

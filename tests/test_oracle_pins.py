@@ -189,6 +189,24 @@ def test_partition_row_ids(oracle_lib, layout):
         assert np.array_equal(scat[r][:, 0, 0], np.array(want[r * T // P:(r + 1) * T // P], np.uint16))
 
 
+@pytest.mark.parametrize("layout,P,cu", [(0, 4, [0, 8, 8, 48, 96]), (1, 3, [0, 5, 50, 51, 96]),
+                                          (0, 1, [0, 10, 12])])
+def test_restore_inverts_partition(oracle_lib, layout, P, cu):
+    o = oracle_lib
+    T = cu[-1]
+    l2g, _ = o.index_map(layout, P, cu, T)
+    rng = np.random.default_rng(2)
+    x = rng.integers(0, 2**16, size=(T, 2, 8), dtype=np.uint16)
+    local = o.partition(l2g, x)
+    assert np.array_equal(o.restore(l2g, local), x)
+    # row ids: global row g of the restored buffer comes from local row g2l[g]
+    ids = np.repeat(np.arange(T, dtype=np.uint16)[:, None], 8, axis=1)
+    want_map = bf.l2g_by_ownership(layout, cu, P, T)
+    back = o.restore(l2g, ids)
+    for q, g in enumerate(want_map):
+        assert back[g, 0] == q
+
+
 # ---------------------------------------------------------------- bf16
 
 
@@ -340,3 +358,45 @@ def test_grad_return_matches_numpy(oracle_lib, layout, P, cu, din, dout):
         else:
             want = torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
             assert np.array_equal(owners[r], want)
+
+
+@pytest.mark.parametrize("din,dout", [("f32", 0), ("bf16", 1), ("bf16", 0)])
+def test_grad_return_accumulate_matches_numpy(oracle_lib, din, dout):
+    o = oracle_lib
+    P, cu = 4, [0, 32, 32, 96]
+    T = cu[-1]
+    rng = np.random.default_rng(9)
+    w32 = [rng.uniform(-1, 1, size=(T, 16)).astype(np.float32) for _ in range(P)]
+    writers = w32 if din == "f32" else [o.f32_to_bf16_array(w) for w in w32]
+    start32 = [rng.uniform(-4, 4, size=(T // P, 16)).astype(np.float32) for _ in range(P)]
+    start = start32 if dout == 0 else [o.f32_to_bf16_array(x) for x in start32]
+    l2g, _ = o.index_map(0, P, cu, T)
+    got = o.grad_return_accumulate(l2g, writers, start)
+    want_map = np.array(bf.l2g_by_ownership(0, cu, P, T), np.int64)
+    wf = [w if din == "f32" else _bf16_to_f32_np(w) for w in writers]
+    for r in range(P):
+        rows = want_map[r * (T // P):(r + 1) * (T // P)]
+        s0 = start[r] if dout == 0 else _bf16_to_f32_np(start[r])
+        ref = _numpy_ordered_sum([s0] + [w[rows] for w in wf])
+        if dout == 0:
+            assert np.array_equal(got[r].view(np.uint32), ref.view(np.uint32))
+        else:
+            want = torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(got[r], want)
+        # the inputs are not modified
+        assert np.array_equal(start[r], start32[r] if dout == 0 else o.f32_to_bf16_array(start32[r]))
+
+
+def test_grad_return_accumulate_closed_forms(oracle_lib):
+    o = oracle_lib
+    P, cu = 3, [0, 12]
+    l2g, _ = o.index_map(0, P, cu, 12)
+    ones = [np.ones((12, 4), np.float32) for _ in range(P)]
+    out = o.grad_return_accumulate(l2g, ones, [np.ones((4, 4), np.float32) for _ in range(P)])
+    assert all(np.all(x == P + 1) for x in out)
+    # order canary: start 2^24, writers (1, -2^24, 1): ((2^24+1)-2^24)+1 = 1,
+    # while adding the start last would give 2
+    big = np.float32(2.0**24)
+    ws = [np.full((12, 4), v, np.float32) for v in (1.0, -big, 1.0)]
+    out = o.grad_return_accumulate(l2g, ws, [np.full((4, 4), big, np.float32) for _ in range(P)])
+    assert all(np.all(x == 1.0) for x in out)
