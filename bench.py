@@ -592,6 +592,19 @@ def run_next_rows(args):
         ms = _median_launch_ms(lambda: cpt.cpt_partition(pl, qkv, out), stream)
         emit(f"partition_policy:{name}", ms, T * (3 * 2 * Hq * D * 2 + 3 * 4), T=T, P=P,
              docs=len(lens), tok_s=T / (ms / 1e3))
+
+    # f2: documents of raw (uneven) lengths: the padded per-document layout
+    # pads on the fly; packed-contiguous needs no padding. Same raw batch.
+    raw = synth.lognormal_doc_lengths(T, synth.rng_for(2, 0), multiple=1)
+    cur = synth.cu_from_lengths(raw)
+    for name, layout in (("per_document_padded", 3), ("packed_contiguous", 1)):
+        pl = cpt.cpt_plan_create(layout, P, cur, T)
+        Tpad = pl.padded_tokens
+        outp = [torch.empty((P, Tpad // P, Hq, D), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        ms = _median_launch_ms(lambda: cpt.cpt_partition(pl, qkv, outp), stream)
+        emit(f"raw_lengths_partition:{name}", ms, 3 * ((T + Tpad) * Hq * D * 2 + Tpad * 4), T=T,
+             T_padded=Tpad, P=P, docs=len(raw), tok_s=T / (ms / 1e3))
+        del outp
     return 0
 
 

@@ -45,6 +45,7 @@ CPT_ERR_NOT_PUBLISHED = 10
 CPT_LAYOUT_DUAL_CHUNK_SWAP = 0
 CPT_LAYOUT_PACKED_CONTIGUOUS = 1
 CPT_LAYOUT_RETIRED_PACKED_SUPER_SEQUENCE = 2
+CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED = 3
 CPT_F32 = 0
 CPT_BF16 = 1
 CPT_WAIT_BOUNDED = 0
@@ -73,6 +74,8 @@ _sig("cpt_plan_create", ctypes.c_int, ctypes.c_int, _i32, _vp, _i32, _i64, _vp, 
      ctypes.POINTER(_vp))
 _sig("cpt_plan_destroy", ctypes.c_int, _vp)
 _sig("cpt_plan_info", ctypes.c_int, _vp, ctypes.POINTER(_i64), ctypes.POINTER(_i32), ctypes.POINTER(_i32))
+_sig("cpt_plan_padded_tokens", ctypes.c_int, _vp, ctypes.POINTER(_i64))
+_sig("cpt_thd_real_lengths", ctypes.c_int, _vp, _vp, _vp)
 _sig("cpt_index_map", ctypes.c_int, _vp, _vp, _vp, _vp)
 _sig("cpt_thd_metadata", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("cpt_partition", ctypes.c_int, _vp, _i32, _vp, _vp, _i64, ctypes.c_int, _vp)
@@ -227,17 +230,18 @@ class Plan:
     """Host handle of a plan plus the workspace tensor it lives in."""
 
     def __init__(self, handle: int, workspace: torch.Tensor, layout: int, cp_size: int,
-                 n_docs: int, total_tokens: int):
+                 n_docs: int, total_tokens: int, padded_tokens: int):
         self.handle = handle
         self.workspace = workspace
         self.layout = layout
         self.cp_size = cp_size
         self.n_docs = n_docs
         self.total_tokens = total_tokens
+        self.padded_tokens = padded_tokens
 
     @property
     def local_tokens(self) -> int:
-        return self.total_tokens // self.cp_size
+        return self.padded_tokens // self.cp_size
 
     def __del__(self):
         h, self.handle = getattr(self, "handle", None), None
@@ -255,7 +259,9 @@ def cpt_plan_create(layout: int, cp_size: int, cu_seqlens, total_tokens: int,
     _check(_lib.cpt_plan_create(layout, cp_size, ctypes.cast(arr, _vp), n, total_tokens,
                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _stream(stream), ctypes.byref(h)))
-    return Plan(h.value, workspace, layout, cp_size, n, total_tokens)
+    tp = _i64()
+    _check(_lib.cpt_plan_padded_tokens(h.value, ctypes.byref(tp)))
+    return Plan(h.value, workspace, layout, cp_size, n, total_tokens, tp.value)
 
 
 def cpt_plan_destroy(plan: Plan) -> None:
@@ -269,6 +275,17 @@ def cpt_plan_info(plan: Plan):
     T, P, n = _i64(), _i32(), _i32()
     _check(_lib.cpt_plan_info(plan.handle, ctypes.byref(T), ctypes.byref(P), ctypes.byref(n)))
     return T.value, P.value, n.value
+
+
+def cpt_plan_padded_tokens(plan: Plan) -> int:
+    v = _i64()
+    _check(_lib.cpt_plan_padded_tokens(plan.handle, ctypes.byref(v)))
+    return v.value
+
+
+def cpt_thd_real_lengths(plan: Plan, real_len: torch.Tensor, stream=None):
+    """real_len[r][i] ([P, n] int32) = real tokens of document i on rank r."""
+    _check(_lib.cpt_thd_real_lengths(plan.handle, _ptr(real_len), _stream(stream)))
 
 
 def cpt_index_map(plan: Plan, l2g: torch.Tensor, g2l: torch.Tensor | None = None, stream=None):

@@ -144,20 +144,34 @@ const DriverOps &driver_ops()
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-    size_t cu, cu_local, num_segs, first, offs, l2g, g2l, total;
+    size_t cu, cup, cu_local, num_segs, first, offs, l2g, g2l, l2r, r2l, total;
 };
 
-WsLayout ws_layout(int P, int n, int64_t T)
+bool is_padded(cpt_layout layout) { return layout == CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED; }
+
+// Largest padded token count for n documents of T tokens: each document
+// grows by at most 2P-1 padding tokens.
+int64_t padded_cap(cpt_layout layout, int P, int n, int64_t T)
 {
+    return is_padded(layout) ? T + (int64_t)n * (2 * P - 1) : T;
+}
+
+WsLayout ws_layout(cpt_layout layout, int P, int n, int64_t T)
+{
+    const int64_t cap = padded_cap(layout, P, n, T);
+    const bool pad = is_padded(layout);
     WsLayout w;
     size_t off = 0;
     w.cu = off;       off += align256(sizeof(int32_t) * (size_t)(n + 1));
+    w.cup = off;      off += pad ? align256(sizeof(int32_t) * (size_t)(n + 1)) : 0;
     w.cu_local = off; off += align256(sizeof(int32_t) * (size_t)P * (size_t)(n + 1));
     w.num_segs = off; off += align256(sizeof(int32_t) * (size_t)P);
     w.first = off;    off += align256(sizeof(int32_t) * (size_t)P);
     w.offs = off;     off += align256(sizeof(int32_t) * (size_t)(P + 1));
-    w.l2g = off;      off += align256(sizeof(int32_t) * (size_t)T);
-    w.g2l = off;      off += align256(sizeof(int32_t) * (size_t)T);
+    w.l2g = off;      off += align256(sizeof(int32_t) * (size_t)cap);
+    w.g2l = off;      off += align256(sizeof(int32_t) * (size_t)cap);
+    w.l2r = off;      off += pad ? align256(sizeof(int32_t) * (size_t)cap) : 0;
+    w.r2l = off;      off += pad ? align256(sizeof(int32_t) * (size_t)T) : 0;
     w.total = off;
     return w;
 }
@@ -169,7 +183,8 @@ cpt_status check_sizes(cpt_layout layout, int32_t P, int32_t n, int64_t T)
                     "layout %d is the retired mirrored packed_super_sequence policy; use "
                     "PACKED_CONTIGUOUS, or a DUAL_CHUNK_SWAP plan over cu_seqlens = {0, T} for "
                     "its map", (int)layout);
-    if (layout != CPT_LAYOUT_DUAL_CHUNK_SWAP && layout != CPT_LAYOUT_PACKED_CONTIGUOUS)
+    if (layout != CPT_LAYOUT_DUAL_CHUNK_SWAP && layout != CPT_LAYOUT_PACKED_CONTIGUOUS &&
+        layout != CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED)
         return fail(CPT_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
     if (P < 1 || P > CPT_MAX_CP_SIZE)
         return fail(CPT_ERR_INVALID_ARG, "cp_size %d outside 1..%d", P, CPT_MAX_CP_SIZE);
@@ -185,14 +200,17 @@ cpt_status check_sizes(cpt_layout layout, int32_t P, int32_t n, int64_t T)
 
 struct cpt_plan {
     cpt_layout layout;
+    int map_layout;   // layout the map and metadata kernels run: padded -> per-document
     int32_t P;
     int32_t n;
-    int64_t T;
-    int64_t Tp;
+    int64_t T;        // tokens of the raw packed buffer
+    int64_t Tpad;     // tokens after padding (= T unless padded)
+    int64_t Tp;       // local tokens per rank, Tpad / P
     int device;
     const uint8_t *ws;
     size_t ws_bytes;
-    int32_t *cu, *cu_local, *num_segs, *first, *offs, *l2g, *g2l;
+    int32_t *cu, *cup, *cu_local, *num_segs, *first, *offs, *l2g, *g2l, *l2r, *r2l;
+    std::vector<int32_t> h_cup;  // host copy of the padded boundaries
 };
 
 struct cpt_epoch {
@@ -277,7 +295,15 @@ cpt_status cpt_validate_layout(cpt_layout layout, int32_t P, const int32_t *cu, 
         if (cu[i + 1] < cu[i])
             return fail(CPT_ERR_INVALID_ARG, "cu_seqlens decreases at %d (%d -> %d)", i, cu[i],
                         cu[i + 1]);
-    if (layout == CPT_LAYOUT_DUAL_CHUNK_SWAP) {
+    if (is_padded(layout)) {
+        int64_t Tpad = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            const int64_t L = cu[i + 1] - cu[i];
+            Tpad += (L + 2 * P - 1) / (2 * P) * (2 * P);
+        }
+        if (Tpad > 0x7FFFFFFF)
+            return fail(CPT_ERR_INVALID_ARG, "padded total %lld exceeds 2^31 - 1", (long long)Tpad);
+    } else if (layout == CPT_LAYOUT_DUAL_CHUNK_SWAP) {
         for (int32_t i = 0; i < n; ++i) {
             const int32_t L = cu[i + 1] - cu[i];
             if (L % (2 * P) != 0)
@@ -295,7 +321,7 @@ cpt_status cpt_validate_layout(cpt_layout layout, int32_t P, const int32_t *cu, 
 size_t cpt_plan_workspace_bytes(cpt_layout layout, int32_t P, int32_t n, int64_t T)
 {
     if (check_sizes(layout, P, n, T) != CPT_OK) return 0;
-    return ws_layout(P, n, T).total;
+    return ws_layout(layout, P, n, T).total;
 }
 
 cpt_status cpt_plan_create(cpt_layout layout, int32_t P, const int32_t *cu, int32_t n, int64_t T,
@@ -307,7 +333,7 @@ cpt_status cpt_plan_create(cpt_layout layout, int32_t P, const int32_t *cu, int3
     if (st) return st;
     int dev = 0;
     if (!current_device(&dev)) return fail(CPT_ERR_CUDA, "cudaGetDevice failed");
-    const WsLayout w = ws_layout(P, n, T);
+    const WsLayout w = ws_layout(layout, P, n, T);
     if (workspace == nullptr) return fail(CPT_ERR_WORKSPACE, "workspace is NULL");
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
         return fail(CPT_ERR_WORKSPACE, "workspace is not 256-byte aligned");
@@ -319,11 +345,12 @@ cpt_status cpt_plan_create(cpt_layout layout, int32_t P, const int32_t *cu, int3
     cpt_plan *p = new (std::nothrow) cpt_plan;
     if (p == nullptr) return fail(CPT_ERR_INVALID_ARG, "out of host memory");
     uint8_t *base = static_cast<uint8_t *>(workspace);
+    const bool pad = is_padded(layout);
     p->layout = layout;
+    p->map_layout = pad ? (int)CPT_LAYOUT_DUAL_CHUNK_SWAP : (int)layout;
     p->P = P;
     p->n = n;
     p->T = T;
-    p->Tp = T / P;
     p->device = dev;
     p->ws = base;
     p->ws_bytes = w.total;
@@ -334,14 +361,39 @@ cpt_status cpt_plan_create(cpt_layout layout, int32_t P, const int32_t *cu, int3
     p->offs = reinterpret_cast<int32_t *>(base + w.offs);
     p->l2g = reinterpret_cast<int32_t *>(base + w.l2g);
     p->g2l = reinterpret_cast<int32_t *>(base + w.g2l);
+    if (pad) {
+        // every document padded up to a multiple of 2P
+        p->h_cup.resize((size_t)n + 1);
+        p->h_cup[0] = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            const int32_t L = cu[i + 1] - cu[i];
+            p->h_cup[i + 1] = p->h_cup[i] + (L + 2 * P - 1) / (2 * P) * (2 * P);
+        }
+        p->Tpad = p->h_cup[n];
+        p->cup = reinterpret_cast<int32_t *>(base + w.cup);
+        p->l2r = reinterpret_cast<int32_t *>(base + w.l2r);
+        p->r2l = reinterpret_cast<int32_t *>(base + w.r2l);
+    } else {
+        p->Tpad = T;
+        p->cup = p->cu;
+        p->l2r = nullptr;
+        p->r2l = nullptr;
+    }
+    p->Tp = p->Tpad / P;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemcpyAsync(p->cu, cu, sizeof(int32_t) * (size_t)(n + 1),
                                     cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = launch_index_map(layout, P, p->cu, n, T, p->l2g, p->g2l, s);
+    if (e == cudaSuccess && pad)
+        e = cudaMemcpyAsync(p->cup, p->h_cup.data(), sizeof(int32_t) * (size_t)(n + 1),
+                            cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)
-        e = launch_thd_metadata(layout, P, p->cu, n, T, p->num_segs, p->first, p->cu_local,
-                                p->offs, s);
+        e = launch_index_map(p->map_layout, P, p->cup, n, p->Tpad, p->l2g, p->g2l, s);
+    if (e == cudaSuccess && pad)
+        e = launch_pad_maps(p->cu, p->cup, n, T, p->Tpad, p->l2g, p->g2l, p->l2r, p->r2l, s);
+    if (e == cudaSuccess)
+        e = launch_thd_metadata(p->map_layout, P, p->cup, n, p->Tpad, p->num_segs, p->first,
+                                p->cu_local, p->offs, s);
     if (e != cudaSuccess) {
         delete p;
         return cuda_fail(e, "plan build");
@@ -365,22 +417,30 @@ cpt_status cpt_plan_info(const cpt_plan *plan, int64_t *T, int32_t *P, int32_t *
     return CPT_OK;
 }
 
+cpt_status cpt_plan_padded_tokens(const cpt_plan *plan, int64_t *padded_total)
+{
+    if (plan == nullptr || padded_total == nullptr)
+        return fail(CPT_ERR_INVALID_ARG, "NULL argument");
+    *padded_total = plan->Tpad;
+    return CPT_OK;
+}
+
 cpt_status cpt_index_map(const cpt_plan *plan, int32_t *l2g, int32_t *g2l, void *stream)
 {
     int dev = 0;
     cpt_status st = check_plan(plan, &dev);
     if (st) return st;
-    if (plan->T == 0) return CPT_OK;
+    if (plan->Tpad == 0) return CPT_OK;
     if ((st = check_ptr(l2g, dev, 4, "l2g"))) return st;
     if (g2l && (st = check_ptr(g2l, dev, 4, "g2l"))) return st;
     std::vector<Range> r;
-    const size_t bytes = sizeof(int32_t) * (size_t)plan->T;
+    const size_t bytes = sizeof(int32_t) * (size_t)plan->Tpad;
     add_range(r, plan->ws, plan->ws_bytes, false, "workspace");
     add_range(r, l2g, bytes, true, "l2g");
     add_range(r, g2l, bytes, true, "g2l");
     if ((st = check_overlaps(r))) return st;
-    cudaError_t e = launch_index_map(plan->layout, plan->P, plan->cu, plan->n, plan->T, l2g, g2l,
-                                     static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_index_map(plan->map_layout, plan->P, plan->cup, plan->n, plan->Tpad, l2g,
+                                     g2l, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CPT_OK : cuda_fail(e, "index map launch");
 }
 
@@ -402,10 +462,27 @@ cpt_status cpt_thd_metadata(const cpt_plan *plan, int32_t *num_segs, int32_t *se
     add_range(r, cu_local, 4 * P * (size_t)(plan->n + 1), true, "cu_local");
     add_range(r, seg_offsets, 4 * (P + 1), true, "seg_offsets");
     if ((st = check_overlaps(r))) return st;
-    cudaError_t e = launch_thd_metadata(plan->layout, plan->P, plan->cu, plan->n, plan->T,
+    cudaError_t e = launch_thd_metadata(plan->map_layout, plan->P, plan->cup, plan->n, plan->Tpad,
                                         num_segs, seg_doc_first, cu_local, seg_offsets,
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CPT_OK : cuda_fail(e, "metadata launch");
+}
+
+cpt_status cpt_thd_real_lengths(const cpt_plan *plan, int32_t *real_len, void *stream)
+{
+    int dev = 0;
+    cpt_status st = check_plan(plan, &dev);
+    if (st) return st;
+    const size_t count = (size_t)plan->P * (size_t)plan->n;
+    if (count == 0) return CPT_OK;
+    if ((st = check_ptr(real_len, dev, 4, "real_len"))) return st;
+    std::vector<Range> r;
+    add_range(r, plan->ws, plan->ws_bytes, false, "workspace");
+    add_range(r, real_len, 4 * count, true, "real_len");
+    if ((st = check_overlaps(r))) return st;
+    cudaError_t e = launch_real_lengths(plan->map_layout, plan->P, plan->cu, plan->cup, plan->n,
+                                        plan->Tpad, real_len, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CPT_OK : cuda_fail(e, "real lengths launch");
 }
 
 static cpt_status check_row(int64_t row_elems, cpt_dtype a, cpt_dtype b, int64_t *units)
@@ -433,7 +510,7 @@ cpt_status cpt_partition(const cpt_plan *plan, int32_t n_tensors, const void *co
     if (src == nullptr || dst == nullptr) return fail(CPT_ERR_INVALID_ARG, "src or dst is NULL");
     int64_t units = 0;
     if ((st = check_row(row_elems, dtype, dtype, &units))) return st;
-    if (plan->T == 0) return CPT_OK;
+    if (plan->Tpad == 0) return CPT_OK;
     const int64_t row_bytes = units * 16;
     std::vector<Range> r;
     add_range(r, plan->ws, plan->ws_bytes, false, "workspace");
@@ -441,21 +518,23 @@ cpt_status cpt_partition(const cpt_plan *plan, int32_t n_tensors, const void *co
         if ((st = check_ptr(src[t], dev, 16, "src", t))) return st;
         if ((st = check_ptr(dst[t], dev, 16, "dst", t))) return st;
         add_range(r, src[t], (size_t)(plan->T * row_bytes), false, "src", t);
-        add_range(r, dst[t], (size_t)(plan->T * row_bytes), true, "dst", t);
+        add_range(r, dst[t], (size_t)(plan->Tpad * row_bytes), true, "dst", t);
     }
     if ((st = check_overlaps(r))) return st;
 
+    // local row q reads raw row l2g[q] (padded layout: l2r[q], -1 = zero row)
     GatherParams p;
     memset(&p, 0, sizeof p);
-    p.l2g = plan->layout == CPT_LAYOUT_PACKED_CONTIGUOUS ? nullptr : plan->l2g;
+    p.l2g = plan->layout == CPT_LAYOUT_PACKED_CONTIGUOUS ? nullptr
+          : (is_padded(plan->layout) ? plan->l2r : plan->l2g);
     for (int t = 0; t < n_tensors; ++t) {
         p.src[t] = static_cast<const uint8_t *>(src[t]);
         for (int o = 0; o < plan->P; ++o)
             p.dst[t][o] = static_cast<uint8_t *>(dst[t]) + (int64_t)o * plan->Tp * row_bytes;
     }
-    p.T = plan->T;
+    p.T = plan->Tpad;
     p.Tp = plan->Tp;
-    p.rows = (int64_t)n_tensors * plan->T;
+    p.rows = (int64_t)n_tensors * plan->Tpad;
     p.units = (int32_t)units;
     p.row_bytes = (int32_t)row_bytes;
     cudaError_t e = launch_gather(p, static_cast<cudaStream_t>(stream));
@@ -480,22 +559,32 @@ cpt_status cpt_restore(const cpt_plan *plan, int32_t n_tensors, const void *cons
     for (int t = 0; t < n_tensors; ++t) {
         if ((st = check_ptr(src[t], dev, 16, "src", t))) return st;
         if ((st = check_ptr(dst[t], dev, 16, "dst", t))) return st;
-        add_range(r, src[t], (size_t)(plan->T * row_bytes), false, "src", t);
+        add_range(r, src[t], (size_t)(plan->Tpad * row_bytes), false, "src", t);
         add_range(r, dst[t], (size_t)(plan->T * row_bytes), true, "dst", t);
     }
     if ((st = check_overlaps(r))) return st;
 
-    // global row g of piece r (g = r*T/P + j) reads local row g2l[g]
     GatherParams p;
     memset(&p, 0, sizeof p);
-    p.l2g = plan->layout == CPT_LAYOUT_PACKED_CONTIGUOUS ? nullptr : plan->g2l;
-    for (int t = 0; t < n_tensors; ++t) {
-        p.src[t] = static_cast<const uint8_t *>(src[t]);
-        for (int o = 0; o < plan->P; ++o)
-            p.dst[t][o] = static_cast<uint8_t *>(dst[t]) + (int64_t)o * plan->Tp * row_bytes;
+    if (is_padded(plan->layout)) {
+        // raw row g reads padded local row r2l[g]; the raw output is one piece
+        p.l2g = plan->r2l;
+        for (int t = 0; t < n_tensors; ++t) {
+            p.src[t] = static_cast<const uint8_t *>(src[t]);
+            p.dst[t][0] = static_cast<uint8_t *>(dst[t]);
+        }
+        p.Tp = plan->T;
+    } else {
+        // global row g of piece r (g = r*T/P + j) reads local row g2l[g]
+        p.l2g = plan->layout == CPT_LAYOUT_PACKED_CONTIGUOUS ? nullptr : plan->g2l;
+        for (int t = 0; t < n_tensors; ++t) {
+            p.src[t] = static_cast<const uint8_t *>(src[t]);
+            for (int o = 0; o < plan->P; ++o)
+                p.dst[t][o] = static_cast<uint8_t *>(dst[t]) + (int64_t)o * plan->Tp * row_bytes;
+        }
+        p.Tp = plan->Tp;
     }
     p.T = plan->T;
-    p.Tp = plan->Tp;
     p.rows = (int64_t)n_tensors * plan->T;
     p.units = (int32_t)units;
     p.row_bytes = (int32_t)row_bytes;
@@ -517,7 +606,7 @@ static cpt_status grad_return_impl(const cpt_plan *plan, const void *const *dkw,
         return fail(CPT_ERR_INVALID_ARG, "dv_writers and dv_owners must both be given or both NULL");
     int64_t units = 0;
     if ((st = check_row(row_elems, in, out, &units))) return st;
-    if (plan->T == 0) return CPT_OK;
+    if (plan->Tpad == 0) return CPT_OK;
     const int nt = dvw ? 2 : 1;
     const int P = plan->P;
     const int64_t in_row = units * 16;
@@ -532,11 +621,12 @@ static cpt_status grad_return_impl(const cpt_plan *plan, const void *const *dkw,
         for (int w = 0; w < P; ++w) {
             if ((st = check_ptr(W[t][w], dev, 16, wn[t], w))) return st;
             if ((st = check_ptr(O[t][w], dev, 16, on[t], w))) return st;
-            add_range(r, W[t][w], (size_t)(plan->T * in_row), false, wn[t], w);
+            add_range(r, W[t][w], (size_t)(plan->Tpad * in_row), false, wn[t], w);
             add_range(r, O[t][w], (size_t)(plan->Tp * out_row), true, on[t], w);
         }
     if ((st = check_overlaps(r))) return st;
 
+    // writers hold the (padded) global layout; owners their local rows
     GradReturnParams p;
     memset(&p, 0, sizeof p);
     p.l2g = plan->l2g;
@@ -545,9 +635,9 @@ static cpt_status grad_return_impl(const cpt_plan *plan, const void *const *dkw,
             p.w[t][w] = static_cast<const uint8_t *>(W[t][w]);
             p.o[t][w] = static_cast<uint8_t *>(O[t][w]);
         }
-    p.T = plan->T;
+    p.T = plan->Tpad;
     p.Tp = plan->Tp;
-    p.rows = (int64_t)nt * plan->T;
+    p.rows = (int64_t)nt * plan->Tpad;
     p.units = (int32_t)units;
     p.in_row_bytes = (int32_t)in_row;
     p.out_row_bytes = (int32_t)out_row;
@@ -585,12 +675,12 @@ cpt_status cpt_grad_scatter(const cpt_plan *plan, int32_t writer, const void *sr
         return fail(CPT_ERR_ALIAS, "slots[%d] does not alias the writer's own local slot", writer);
     int64_t units = 0;
     if ((st = check_row(row_elems, dtype, dtype, &units))) return st;
-    if (plan->T == 0) return CPT_OK;
+    if (plan->Tpad == 0) return CPT_OK;
     const int64_t row_bytes = units * 16;
     std::vector<Range> r;
     add_range(r, plan->ws, plan->ws_bytes, false, "workspace");
     if ((st = check_ptr(src, dev, 16, "src"))) return st;
-    add_range(r, src, (size_t)(plan->T * row_bytes), false, "src");
+    add_range(r, src, (size_t)(plan->Tpad * row_bytes), false, "src");
     for (int o = 0; o < P; ++o) {
         if ((st = check_ptr(slots[o], dev, 16, "slots", o))) return st;
         add_range(r, slots[o], (size_t)(plan->Tp * row_bytes), true, "slots", o);
@@ -602,9 +692,9 @@ cpt_status cpt_grad_scatter(const cpt_plan *plan, int32_t writer, const void *sr
     p.l2g = plan->layout == CPT_LAYOUT_PACKED_CONTIGUOUS ? nullptr : plan->l2g;
     p.src[0] = static_cast<const uint8_t *>(src);
     for (int o = 0; o < P; ++o) p.dst[0][o] = static_cast<uint8_t *>(slots[o]);
-    p.T = plan->T;
+    p.T = plan->Tpad;
     p.Tp = plan->Tp;
-    p.rows = plan->T;
+    p.rows = plan->Tpad;
     p.units = (int32_t)units;
     p.row_bytes = (int32_t)row_bytes;
     cudaError_t e = launch_gather(p, static_cast<cudaStream_t>(stream));
@@ -849,11 +939,27 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
 {
     cpt_status st = cpt_validate_layout(layout, P, cu, n, T);
     if (st) return st;
-    if (T > CPT_NOALLOC_MAX_TOKENS)
+    // the padded layout is the per-document one over padded boundaries
+    std::vector<int32_t> cup;
+    const int32_t *cu_map = cu;
+    int64_t Tmap = T;
+    int map_layout = (int)layout;
+    if (is_padded(layout)) {
+        cup.resize((size_t)n + 1);
+        cup[0] = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            const int32_t L = cu[i + 1] - cu[i];
+            cup[i + 1] = cup[i] + (L + 2 * P - 1) / (2 * P) * (2 * P);
+        }
+        cu_map = cup.data();
+        Tmap = cup[n];
+        map_layout = (int)CPT_LAYOUT_DUAL_CHUNK_SWAP;
+    }
+    if (Tmap > CPT_NOALLOC_MAX_TOKENS)
         return fail(CPT_ERR_INVALID_ARG,
                     "total_tokens %lld exceeds the no-allocation limit of %d tokens "
                     "(use cpt_plan_create with a workspace)",
-                    (long long)T, CPT_NOALLOC_MAX_TOKENS);
+                    (long long)Tmap, CPT_NOALLOC_MAX_TOKENS);
     if (n > CPT_NOALLOC_MAX_DOCS)
         return fail(CPT_ERR_INVALID_ARG,
                     "n_docs %d exceeds the no-allocation limit of %d documents "
@@ -869,10 +975,10 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
     if (!current_device(&dev)) return fail(CPT_ERR_CUDA, "cudaGetDevice failed");
     int32_t *scratch = nullptr;
     if ((st = noalloc_scratch(dev, &scratch))) return st;
-    if (T == 0) return CPT_OK;
+    if (Tmap == 0) return CPT_OK;
 
     const int nt = dvw ? 2 : 1;
-    const int64_t Tp = T / P;
+    const int64_t Tp = Tmap / P;
     const int64_t in_row = units * 16;
     const int64_t out_row = row_elems * (int64_t)dtype_size(out);
     const void *const *W[2] = {dkw, dvw};
@@ -886,7 +992,7 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
         for (int w = 0; w < P; ++w) {
             if ((st = check_ptr(W[t][w], dev, 16, wn[t], w))) return st;
             if ((st = check_ptr(O[t][w], dev, 16, on[t], w))) return st;
-            add_range(r, W[t][w], (size_t)(T * in_row), false, wn[t], w);
+            add_range(r, W[t][w], (size_t)(Tmap * in_row), false, wn[t], w);
             add_range(r, O[t][w], (size_t)(Tp * out_row), true, on[t], w);
         }
     if ((st = check_overlaps(r))) return st;
@@ -896,9 +1002,9 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
     int32_t *d_cu = scratch;
     int32_t *d_l2g = scratch + kNoAllocCuSlots;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemcpyAsync(d_cu, cu, sizeof(int32_t) * (size_t)(n + 1),
+    cudaError_t e = cudaMemcpyAsync(d_cu, cu_map, sizeof(int32_t) * (size_t)(n + 1),
                                     cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = launch_index_map(layout, P, d_cu, n, T, d_l2g, nullptr, s);
+    if (e == cudaSuccess) e = launch_index_map(map_layout, P, d_cu, n, Tmap, d_l2g, nullptr, s);
     if (e != cudaSuccess) return cuda_fail(e, "no-allocation map build");
 
     GradReturnParams p;
@@ -909,9 +1015,9 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
             p.w[t][w] = static_cast<const uint8_t *>(W[t][w]);
             p.o[t][w] = static_cast<uint8_t *>(O[t][w]);
         }
-    p.T = T;
+    p.T = Tmap;
     p.Tp = Tp;
-    p.rows = (int64_t)nt * T;
+    p.rows = (int64_t)nt * Tmap;
     p.units = (int32_t)units;
     p.in_row_bytes = (int32_t)in_row;
     p.out_row_bytes = (int32_t)out_row;

@@ -10,7 +10,7 @@ namespace cpt {
 constexpr int kMaxCp = 8;        // largest cp_size (one pointer slot per rank)
 constexpr int kMaxTensors = 3;   // Q, K, V in one gather launch
 
-enum Layout : int { kDualChunkSwap = 0, kPackedContiguous = 1 };
+enum Layout : int { kDualChunkSwap = 0, kPackedContiguous = 1, kDualChunkSwapPadded = 3 };
 enum Dtype : int { kF32 = 0, kBf16 = 1 };
 
 // Status codes a kernel may write to a device status word (mirror cpt.h).
@@ -29,7 +29,18 @@ cudaError_t launch_thd_metadata(int layout, int cp_size, const int32_t *cu, int 
                                 int64_t T, int32_t *num_segs, int32_t *seg_doc_first,
                                 int32_t *cu_local, int32_t *seg_offsets, cudaStream_t stream);
 
-// a4/a6: dst[t][r][j] = src[t][l2g[r*Tp + j]] (bit copy of 16-byte units).
+// Padded layout maps: l2r[q] = raw row of padded local row q (-1: padding),
+// r2l[g] = padded local row of raw row g.
+cudaError_t launch_pad_maps(const int32_t *cu, const int32_t *cup, int n_docs, int64_t T,
+                            int64_t Tpad, const int32_t *l2g_padded, const int32_t *g2l_padded,
+                            int32_t *l2r, int32_t *r2l, cudaStream_t stream);
+
+// real_len[r][i] = real tokens of document i on rank r (cup = cu if unpadded).
+cudaError_t launch_real_lengths(int layout, int cp_size, const int32_t *cu, const int32_t *cup,
+                                int n_docs, int64_t Tpad, int32_t *real_len, cudaStream_t stream);
+
+// a4/a6: dst[t][r][j] = src[t][l2g[r*Tp + j]] (bit copy of 16-byte units); a
+// negative index writes a zero row (padding).
 struct GatherParams {
     const int32_t *l2g;                  // nullptr: identity map
     const uint8_t *src[kMaxTensors];     // [T][row_bytes]

@@ -5,7 +5,8 @@
 //  - its inverse after an all-gather, back to global order: index = g2l;
 //  - the per-writer scatter into owner slots of "Add stream-ordered CP
 //    gradient return primitive" (TransformerEngine PR 3235, sequence diagram):
-//    index = l2g, one destination pointer per owner.
+//    index = l2g, one destination pointer per owner;
+//  - the padded layout: index -1 marks a padding row, written as zeros.
 //
 // HBM-bound bit copy: every output row is one source row. A warp owns one row
 // at a time and moves it in 16-byte units, kUnroll units per lane in flight
@@ -34,8 +35,12 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p)
         const int r = (int)(q / p.Tp);
         const int64_t j = q - (int64_t)r * p.Tp;
         const int64_t g = p.l2g ? (int64_t)__ldg(p.l2g + q) : q;
-        const uint8_t *src = p.src[t] + g * p.row_bytes;
         uint8_t *dst = p.dst[t][r] + j * p.row_bytes;
+        if (g < 0) {  // padding row of the padded layout
+            for (int u = lane; u < units; u += 32) st_once(dst + (int64_t)u * 16, make_uint4(0, 0, 0, 0));
+            continue;
+        }
+        const uint8_t *src = p.src[t] + g * p.row_bytes;
 
         for (int u0 = lane; u0 < units; u0 += 32 * kUnroll) {
             uint4 v[kUnroll];

@@ -110,6 +110,69 @@ __global__ void thd_metadata_kernel(int layout, int P, const int32_t *__restrict
     }
 }
 
+// Padded per-document layout: documents are padded up to multiples of 2P
+// (cup = padded prefix sums). l2r[q]: raw row held by padded local row q, or
+// -1 for padding; r2l[g]: padded local row holding raw row g.
+__global__ void pad_maps_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ cup,
+                                int n, int64_t T, int64_t Tpad,
+                                const int32_t *__restrict__ l2g_padded,
+                                const int32_t *__restrict__ g2l_padded, int32_t *__restrict__ l2r,
+                                int32_t *__restrict__ r2l)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < Tpad; q += stride) {
+        const int64_t gp = __ldg(l2g_padded + q);
+        int lo = 0, hi = n;  // last i with cup[i] <= gp (gp < cup[n] = Tpad)
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(cup + mid) <= gp) lo = mid; else hi = mid;
+        }
+        const int64_t u = gp - __ldg(cup + lo);
+        const int64_t L = __ldg(cu + lo + 1) - __ldg(cu + lo);
+        l2r[q] = u < L ? (int32_t)(__ldg(cu + lo) + u) : -1;
+    }
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < T; g += stride) {
+        int lo = 0, hi = n;  // last i with cu[i] <= g (g < cu[n] = T)
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(cu + mid) <= g) lo = mid; else hi = mid;
+        }
+        r2l[g] = __ldg(g2l_padded + __ldg(cup + lo) + (g - __ldg(cu + lo)));
+    }
+}
+
+// real_len[r][i]: real tokens of document i on rank r. Per-document layouts
+// (cup = cu when unpadded): the rank's chunks r and 2P-1-r of the padded
+// document, each clipped to the real length. Packed: the document's overlap
+// with the rank's contiguous chunk.
+__global__ void real_lengths_kernel(int layout, int P, const int32_t *__restrict__ cu,
+                                    const int32_t *__restrict__ cup, int n, int64_t Tpad,
+                                    int32_t *__restrict__ real_len)
+{
+    const int64_t total = (int64_t)P * n;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total; k += stride) {
+        const int r = (int)(k / n);
+        const int i = (int)(k - (int64_t)r * n);
+        const int64_t c0 = __ldg(cu + i), L = __ldg(cu + i + 1) - c0;
+        int64_t v = 0;
+        if (layout == kPackedContiguous) {
+            const int64_t Tp = Tpad / P, a = (int64_t)r * Tp, b = a + Tp;
+            const int64_t lo = c0 > a ? c0 : a, hi = c0 + L < b ? c0 + L : b;
+            v = hi > lo ? hi - lo : 0;
+        } else {
+            const int64_t mp = (__ldg(cup + i + 1) - __ldg(cup + i)) / (2 * P);
+            const int64_t ks[2] = {r, 2 * P - 1 - r};
+            for (int h = 0; h < 2; ++h) {
+                int64_t c = L - ks[h] * mp;
+                c = c < 0 ? 0 : (c > mp ? mp : c);
+                v += c;
+            }
+        }
+        real_len[k] = (int32_t)v;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_index_map(int layout, int cp_size, const int32_t *cu, int n_docs, int64_t T,
@@ -131,6 +194,38 @@ cudaError_t launch_thd_metadata(int layout, int cp_size, const int32_t *cu, int 
 {
     thd_metadata_kernel<<<1, 32 * kMaxCp, 0, stream>>>(layout, cp_size, cu, n_docs, T, num_segs,
                                                         seg_doc_first, cu_local, seg_offsets);
+    return cudaGetLastError();
+}
+
+}  // namespace cpt
+
+namespace cpt {
+
+cudaError_t launch_pad_maps(const int32_t *cu, const int32_t *cup, int n_docs, int64_t T,
+                            int64_t Tpad, const int32_t *l2g_padded, const int32_t *g2l_padded,
+                            int32_t *l2r, int32_t *r2l, cudaStream_t stream)
+{
+    const int64_t work = Tpad > T ? Tpad : T;
+    if (work == 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = (work + threads - 1) / threads;
+    const int64_t cap = (int64_t)sm_count(-1) * 8;
+    if (blocks > cap) blocks = cap;
+    pad_maps_kernel<<<(unsigned)blocks, threads, 0, stream>>>(cu, cup, n_docs, T, Tpad, l2g_padded,
+                                                              g2l_padded, l2r, r2l);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_real_lengths(int layout, int cp_size, const int32_t *cu, const int32_t *cup,
+                                int n_docs, int64_t Tpad, int32_t *real_len, cudaStream_t stream)
+{
+    const int64_t total = (int64_t)cp_size * n_docs;
+    if (total == 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 1024) blocks = 1024;
+    real_lengths_kernel<<<(unsigned)blocks, threads, 0, stream>>>(layout, cp_size, cu, cup, n_docs,
+                                                                  Tpad, real_len);
     return cudaGetLastError();
 }
 

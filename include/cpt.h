@@ -87,10 +87,20 @@ typedef enum cpt_status {
  *  PACKED_CONTIGUOUS  the whole packed buffer is cut into P equal contiguous
  *                     chunks, rank r owning the r-th; document boundaries
  *                     survive only through the metadata. T must divide by P.
+ *  DUAL_CHUNK_SWAP_PADDED
+ *                     per document, for documents of any length: each is
+ *                     padded up to the next multiple of 2P (the padded
+ *                     boundaries cu_padded are the prefix sums of the padded
+ *                     lengths), then split as DUAL_CHUNK_SWAP over cu_padded.
+ *                     This is the variant [TE-3221] "Why" contrasts with the
+ *                     packed policy. T_pad = cu_padded[n] (see
+ *                     cpt_plan_padded_tokens); local buffers hold T_pad/P rows
+ *                     per rank, padding rows included.
  */
 typedef enum cpt_layout {
     CPT_LAYOUT_DUAL_CHUNK_SWAP = 0,
-    CPT_LAYOUT_PACKED_CONTIGUOUS = 1
+    CPT_LAYOUT_PACKED_CONTIGUOUS = 1,
+    CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED = 3
 } cpt_layout;
 
 /* The mirrored "packed_super_sequence" policy (2P chunks over the whole
@@ -145,12 +155,15 @@ CPT_API const char *cpt_status_string(cpt_status status);
  *  layout, n_docs < 0, total_tokens outside [0, 2^31), or malformed
  *  cu_seqlens; CPT_ERR_NOT_DIVISIBLE when a document length is not a
  *  multiple of 2*cp_size (DUAL_CHUNK_SWAP) or total_tokens is not a
- *  multiple of cp_size (PACKED_CONTIGUOUS). */
+ *  multiple of cp_size (PACKED_CONTIGUOUS); DUAL_CHUNK_SWAP_PADDED accepts
+ *  any lengths whose padded total stays below 2^31. */
 CPT_API cpt_status cpt_validate_layout(cpt_layout layout, int32_t cp_size, const int32_t *cu_seqlens_host,
                                int32_t n_docs, int64_t total_tokens);
 
 /* Device workspace bytes a plan needs (its maps and metadata), or 0 for
- * arguments that cpt_validate_layout would reject on size grounds. */
+ * arguments that cpt_validate_layout would reject on size grounds. For
+ * DUAL_CHUNK_SWAP_PADDED it is sized for the largest possible padding,
+ * total_tokens + n_docs * (2*cp_size - 1). */
 CPT_API size_t cpt_plan_workspace_bytes(cpt_layout layout, int32_t cp_size, int32_t n_docs,
                                 int64_t total_tokens);
 
@@ -185,15 +198,20 @@ CPT_API cpt_status cpt_plan_destroy(cpt_plan *plan);
 CPT_API cpt_status cpt_plan_info(const cpt_plan *plan, int64_t *total_tokens, int32_t *cp_size,
                          int32_t *n_docs);
 
+/* Tokens of the (padded) buffer the plan partitions: T_pad for
+ * DUAL_CHUNK_SWAP_PADDED, T otherwise. Local buffers have T_pad/P rows per
+ * rank. Host only. */
+CPT_API cpt_status cpt_plan_padded_tokens(const cpt_plan *plan, int64_t *padded_total);
+
 /* ------------------------------------------------------------------ */
 /* Ownership maps                                                      */
 /* ------------------------------------------------------------------ */
 
 /* Write the local-to-global map and its inverse ([TE-3235] author's reply,
  * [TE-3221] "Why").
- *  l2g  device int32[T]: l2g[q] = global token held at flattened local
- *       index q = r*T/P + j.
- *  g2l  device int32[T] or NULL: g2l[l2g[q]] = q.
+ *  l2g  device int32[T_pad]: l2g[q] = global token held at flattened local
+ *       index q = r*T_pad/P + j (a padded position for the padded layout).
+ *  g2l  device int32[T_pad] or NULL: g2l[l2g[q]] = q.
  *  DUAL_CHUNK_SWAP, document i with m = L_i/(2P) and local offset
  *  u = j - cu[i]/P inside it: l2g = cu[i] + r*m + u when u < m, else
  *  cu[i] + (2P-1-r)*m + (u-m). PACKED_CONTIGUOUS: l2g[q] = q (rank-major
@@ -219,11 +237,22 @@ CPT_API cpt_status cpt_index_map(const cpt_plan *plan, int32_t *l2g, int32_t *g2
  *                     num_segs[r] on are T/P.
  *  seg_offsets[P+1]   exclusive prefix sum of num_segs.
  *  DUAL_CHUNK_SWAP: every rank has all n documents, cu_local = cu/P.
+ *  DUAL_CHUNK_SWAP_PADDED: the same over the padded boundaries,
+ *  cu_local = cu_padded/P (cpt_thd_real_lengths gives the real tokens).
  *  PACKED_CONTIGUOUS: the non-empty pieces of the documents inside
  *  [r*T/P, (r+1)*T/P), in document order, offsets relative to r*T/P.
  *  Errors: as cpt_index_map. */
 CPT_API cpt_status cpt_thd_metadata(const cpt_plan *plan, int32_t *num_segs, int32_t *seg_doc_first,
                             int32_t *cu_local, int32_t *seg_offsets, void *stream);
+
+/* Real (non-padding) tokens of every document on every rank:
+ *  real_len  device int32[P][n]: real_len[r][i] = tokens of document i that
+ *            rank r holds. Per-document layouts: the rank's chunks r and
+ *            2P-1-r of the (padded) document, each clipped to the document's
+ *            real length; packed: the document's overlap with the rank's
+ *            chunk. Each column sums to the document's length.
+ *  Errors: as cpt_index_map. */
+CPT_API cpt_status cpt_thd_real_lengths(const cpt_plan *plan, int32_t *real_len, void *stream);
 
 /* ------------------------------------------------------------------ */
 /* Q/K/V reorder                                                       */
@@ -234,9 +263,9 @@ CPT_API cpt_status cpt_thd_metadata(const cpt_plan *plan, int32_t *num_segs, int
  * kernels ..."): dst[t][r][j] = src[t][l2g[r*T/P + j]], a bit copy.
  *  n_tensors  1..3 (Q, K, V).
  *  src        host array of n_tensors device pointers, each [T][row].
- *  dst        host array of n_tensors device pointers, each [P][T/P][row]
+ *  dst        host array of n_tensors device pointers, each [P][T_pad/P][row]
  *             (contiguous rank-major); must not overlap any src or another
- *             dst.
+ *             dst. Padding rows of the padded layout are written as zeros.
  *  row_elems  elements per token row (H*D); row bytes must be a multiple
  *             of 16.
  *  Errors: CPT_ERR_INVALID_ARG, CPT_ERR_DEVICE, CPT_ERR_ALIGNMENT,
@@ -249,10 +278,11 @@ CPT_API cpt_status cpt_partition(const cpt_plan *plan, int32_t n_tensors, const 
  * CP; commit "Allow relaxed THD all-gather ...": rank-major ownership is the
  * policy that needs no KV reorder, so the per-document one does):
  *   dst[t][g] = src[t][g2l[g]], i.e. dst[t][l2g[q]] = src[t][q], a bit copy.
- *  src        host array of n_tensors device pointers, each [P][T/P][row]
+ *  src        host array of n_tensors device pointers, each [P][T_pad/P][row]
  *             (the all-gathered rank-major buffer).
- *  dst        host array of n_tensors device pointers, each [T][row]; must
- *             not overlap any src or another dst.
+ *  dst        host array of n_tensors device pointers, each [T][row] (raw
+ *             order; the padded layout drops its padding rows); must not
+ *             overlap any src or another dst.
  *  Other arguments and errors: as cpt_partition. */
 CPT_API cpt_status cpt_restore(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
                                void *const *dst, int64_t row_elems, cpt_dtype dtype, void *stream);
@@ -270,8 +300,9 @@ CPT_API cpt_status cpt_restore(const cpt_plan *plan, int32_t n_tensors, const vo
  * binary32 adds in writer order with the accumulator starting at x_0, then
  * one rounding to the output type (round-to-nearest-even for bf16). The
  * owner buffers are overwritten.
- *  dk_writers  host array of P device pointers, writer w's global [T][row].
- *  dk_owners   host array of P device pointers, owner o's local [T/P][row].
+ *  dk_writers  host array of P device pointers, writer w's global [T_pad][row]
+ *              (for the padded layout: the padded global order).
+ *  dk_owners   host array of P device pointers, owner o's local [T_pad/P][row].
  *  dv_writers, dv_owners  the same for dV, or both NULL to return dK only.
  *  in, out     element types of writers and owners.
  *  Errors: CPT_ERR_INVALID_ARG (one of the dV pair NULL), CPT_ERR_DEVICE,

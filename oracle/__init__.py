@@ -76,6 +76,17 @@ def _load():
             lib.oracle_partition.restype = None
             lib.oracle_restore.argtypes = [i32p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
             lib.oracle_restore.restype = None
+            lib.oracle_pad_cu.argtypes = [ctypes.c_int, i32p, ctypes.c_int, i32p]
+            lib.oracle_pad_cu.restype = None
+            lib.oracle_partition_padded.argtypes = [i32p, ctypes.c_int64, i32p, i32p, ctypes.c_int,
+                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+            lib.oracle_partition_padded.restype = None
+            lib.oracle_restore_padded.argtypes = [i32p, i32p, i32p, ctypes.c_int, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_int64]
+            lib.oracle_restore_padded.restype = None
+            lib.oracle_real_lengths.argtypes = [ctypes.c_int, i32p, ctypes.c_int64, i32p, i32p, ctypes.c_int,
+                                                i32p]
+            lib.oracle_real_lengths.restype = None
             lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
             lib.oracle_bf16_to_f32.restype = ctypes.c_float
             lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -174,6 +185,61 @@ def restore(l2g: np.ndarray, local: np.ndarray) -> np.ndarray:
     out = np.empty_like(local)
     row_bytes = local.nbytes // T if T else 0
     _load().oracle_restore(_ptr(l2g), T, _ptr(local), _ptr(out), row_bytes)
+    return out
+
+
+def pad_cu(cp_size: int, cu_seqlens) -> np.ndarray:
+    """cu_seqlens with every document padded up to a multiple of 2P."""
+    cu = _cu(cu_seqlens)
+    out = np.empty_like(cu)
+    _load().oracle_pad_cu(cp_size, _ptr(cu), len(cu) - 1, _ptr(out))
+    return out
+
+
+def padded_index_map(cp_size: int, cu_seqlens):
+    """(cu_padded, l2g, g2l) of the padded per-document layout (T_pad tokens)."""
+    cup = pad_cu(cp_size, cu_seqlens)
+    l2g, g2l = index_map(LAYOUT_DSC, cp_size, cup, int(cup[-1]))
+    return cup, l2g, g2l
+
+
+def partition_padded(cp_size: int, cu_seqlens, src: np.ndarray) -> np.ndarray:
+    """Rank-local [T_pad, ...] from raw [T, ...], padding rows zero."""
+    cu = _cu(cu_seqlens)
+    cup, l2g, _ = padded_index_map(cp_size, cu)
+    src = np.ascontiguousarray(src)
+    Tpad = int(cup[-1])
+    dst = np.empty((Tpad,) + src.shape[1:], src.dtype)
+    row_bytes = int(np.prod(src.shape[1:], dtype=np.int64)) * src.itemsize
+    _load().oracle_partition_padded(_ptr(l2g), Tpad, _ptr(cu), _ptr(cup), len(cu) - 1, _ptr(src),
+                                    _ptr(dst), row_bytes)
+    return dst
+
+
+def restore_padded(cp_size: int, cu_seqlens, local: np.ndarray) -> np.ndarray:
+    """Raw [T, ...] from the rank-local padded [T_pad, ...] (padding dropped)."""
+    cu = _cu(cu_seqlens)
+    cup, _, g2l = padded_index_map(cp_size, cu)
+    local = np.ascontiguousarray(local)
+    T = int(cu[-1])
+    out = np.empty((T,) + local.shape[1:], local.dtype)
+    row_bytes = int(np.prod(local.shape[1:], dtype=np.int64)) * local.itemsize
+    _load().oracle_restore_padded(_ptr(g2l), _ptr(cu), _ptr(cup), len(cu) - 1, _ptr(local), _ptr(out),
+                                  row_bytes)
+    return out
+
+
+def real_lengths(layout: int, cp_size: int, cu_seqlens, padded: bool = False) -> np.ndarray:
+    """[P][n]: real tokens of document i held by rank r."""
+    cu = _cu(cu_seqlens)
+    n = len(cu) - 1
+    if padded:
+        cup, l2g, _ = padded_index_map(cp_size, cu)
+    else:
+        cup = cu
+        l2g, _ = index_map(layout, cp_size, cu, int(cu[-1]))
+    out = np.empty((cp_size, n), np.int32)
+    _load().oracle_real_lengths(cp_size, _ptr(l2g), int(cup[-1]), _ptr(cu), _ptr(cup), n, _ptr(out))
     return out
 
 

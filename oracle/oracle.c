@@ -206,6 +206,85 @@ void oracle_restore(const int32_t *l2g, int64_t T, const void *local, void *glob
 }
 
 /* ------------------------------------------------------------------ */
+/* Padded per-document layout: documents whose length is not a multiple */
+/* of 2P ([TE-3221] "Why": the per-document partition cannot split     */
+/* them) are each padded up to the next multiple of 2P. cu_padded is    */
+/* the prefix sum of the padded lengths; the per-document DualChunkSwap */
+/* partition then runs over cu_padded. Padding positions hold no token. */
+/* Parity: pinned (divisible documents reduce to the plain layout,     */
+/* round trip, zero padding rows, brute-force real-token counts).      */
+/* ------------------------------------------------------------------ */
+void oracle_pad_cu(int P, const int32_t *cu, int n, int32_t *cu_padded)
+{
+    cu_padded[0] = 0;
+    for (int i = 0; i < n; ++i) {
+        int32_t L = cu[i + 1] - cu[i];
+        int32_t Lp = ((L + 2 * P - 1) / (2 * P)) * (2 * P);
+        cu_padded[i + 1] = cu_padded[i] + Lp;
+    }
+}
+
+/* Raw row held at padded global position gp, or -1 for padding. */
+static int64_t raw_of_padded(const int32_t *cu, const int32_t *cup, int n, int64_t gp)
+{
+    for (int i = 0; i < n; ++i) {
+        if (gp >= cup[i] && gp < cup[i + 1]) {
+            int64_t u = gp - cup[i];
+            return (u < (int64_t)(cu[i + 1] - cu[i])) ? (int64_t)cu[i] + u : -1;
+        }
+    }
+    return -1;
+}
+
+/* Partition with padding: local row q of the padded layout receives raw row
+ * raw_of_padded(l2g_padded[q]), or zero bytes for padding. Tp = Tpad/P. */
+void oracle_partition_padded(const int32_t *l2g_padded, int64_t Tpad, const int32_t *cu,
+                             const int32_t *cup, int n, const void *src, void *dst,
+                             int64_t row_bytes)
+{
+    const uint8_t *s = (const uint8_t *)src;
+    uint8_t *d = (uint8_t *)dst;
+    for (int64_t q = 0; q < Tpad; ++q) {
+        int64_t g = raw_of_padded(cu, cup, n, l2g_padded[q]);
+        if (g >= 0) memcpy(d + q * row_bytes, s + g * row_bytes, (size_t)row_bytes);
+        else memset(d + q * row_bytes, 0, (size_t)row_bytes);
+    }
+}
+
+/* Un-pad after an all-gather: raw row g of document i sits at padded
+ * position cup[i] + (g - cu[i]), which local row g2l_padded[...] holds. */
+void oracle_restore_padded(const int32_t *g2l_padded, const int32_t *cu, const int32_t *cup,
+                           int n, const void *local, void *raw, int64_t row_bytes)
+{
+    const uint8_t *s = (const uint8_t *)local;
+    uint8_t *d = (uint8_t *)raw;
+    for (int i = 0; i < n; ++i)
+        for (int64_t g = cu[i]; g < cu[i + 1]; ++g) {
+            int64_t q = g2l_padded[cup[i] + (g - cu[i])];
+            memcpy(d + g * row_bytes, s + q * row_bytes, (size_t)row_bytes);
+        }
+}
+
+/* Real (non-padding) tokens of document i on rank r, real_len[r*n + i], by
+ * walking the rank's local rows through the map. Works for every layout:
+ * pass cup = cu for the unpadded ones. */
+void oracle_real_lengths(int P, const int32_t *l2g, int64_t Tpad, const int32_t *cu,
+                         const int32_t *cup, int n, int32_t *real_len)
+{
+    int64_t Tp = Tpad / P;
+    for (int64_t k = 0; k < (int64_t)P * n; ++k) real_len[k] = 0;
+    for (int r = 0; r < P; ++r)
+        for (int64_t j = 0; j < Tp; ++j) {
+            int64_t gp = l2g[(int64_t)r * Tp + j];
+            for (int i = 0; i < n; ++i)
+                if (gp >= cup[i] && gp < cup[i + 1]) {
+                    if (gp - cup[i] < (int64_t)(cu[i + 1] - cu[i])) real_len[r * n + i] += 1;
+                    break;
+                }
+        }
+}
+
+/* ------------------------------------------------------------------ */
 /* bf16 <-> f32.                                                       */
 /* bf16 is the top half of a binary32 word, so widening is exact.      */
 /* Narrowing rounds to nearest, ties to even, from the bit definition: */

@@ -73,7 +73,7 @@ def test_validate_layout_agrees_with_oracle(cpt, oracle_lib, layout):
 def test_validate_layout_rejects_bad_arguments(cpt):
     assert cpt.cpt_validate_layout(0, 0, [0, 8], 8) == cpt.CPT_ERR_INVALID_ARG
     assert cpt.cpt_validate_layout(0, 9, [0, 18], 18) == cpt.CPT_ERR_INVALID_ARG
-    assert cpt.cpt_validate_layout(3, 2, [0, 8], 8) == cpt.CPT_ERR_INVALID_ARG
+    assert cpt.cpt_validate_layout(7, 2, [0, 8], 8) == cpt.CPT_ERR_INVALID_ARG
     assert cpt.cpt_validate_layout(0, 2, [0, 6], 6) == cpt.CPT_ERR_NOT_DIVISIBLE
     assert "not a multiple" in cpt.cpt_last_error_string()
     assert cpt.cpt_validate_layout(1, 4, [0, 6], 6) == cpt.CPT_ERR_NOT_DIVISIBLE
@@ -97,7 +97,7 @@ def test_retired_packed_super_sequence_selector_is_rejected(cpt):
     assert cpt.cpt_validate_layout(code, 4, [0, 64], 64) == cpt.CPT_ERR_UNSUPPORTED
     assert "retired" in cpt.cpt_last_error_string()
     assert cpt.cpt_plan_workspace_bytes(code, 4, 1, 64) == 0
-    assert cpt.cpt_validate_layout(3, 4, [0, 64], 64) == cpt.CPT_ERR_INVALID_ARG
+    assert cpt.cpt_validate_layout(7, 4, [0, 64], 64) == cpt.CPT_ERR_INVALID_ARG
 
 
 def test_mirrored_map_is_dsc_over_one_sequence(oracle_lib):
@@ -114,3 +114,15 @@ def test_mirrored_map_is_dsc_over_one_sequence(oracle_lib):
             want = list(range(r * m, (r + 1) * m)) + list(range((2 * P - 1 - r) * m, (2 * P - r) * m))
             assert l2g[r * 2 * m:(r + 1) * 2 * m].tolist() == want
         assert np.array_equal(np.sort(l2g), np.arange(T))
+
+
+def test_padded_layout_validation(cpt):
+    """The padded per-document layout takes documents of any length."""
+    PAD = cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED
+    assert cpt.cpt_validate_layout(PAD, 4, [0, 5, 5, 12], 12) == cpt.CPT_OK
+    assert cpt.cpt_validate_layout(0, 4, [0, 5, 5, 12], 12) == cpt.CPT_ERR_NOT_DIVISIBLE
+    assert cpt.cpt_validate_layout(PAD, 4, [0, 5, 3], 3) == cpt.CPT_ERR_INVALID_ARG
+    # workspace sized for the largest padding: n * (2P - 1) extra tokens
+    assert cpt.cpt_plan_workspace_bytes(PAD, 4, 3, 12) >= cpt.cpt_plan_workspace_bytes(0, 4, 3, 12)
+    big = 2**31 - 8
+    assert cpt.cpt_validate_layout(PAD, 8, [0, 1, big], big) == cpt.CPT_ERR_INVALID_ARG

@@ -409,3 +409,85 @@ def test_rejections_leave_outputs_untouched(cpt, cuda_device):
     expect(cpt.CPT_ERR_ALIAS, lambda: cpt.cpt_partition(plan, [q], [q.view(P, 16, 16)]))
     torch.cuda.synchronize()
     assert bool((o == 3.0).all().item())
+
+
+# ---------------------------------------------------------------- padded layout
+
+PADDED = 3
+PAD_CASES = [
+    (2, [5, 0, 7], (2, 8), "f32"),
+    (4, [1, 8, 13, 0, 2047, 3], (3, 40), "bf16"),
+    (8, [100, 17], (20, 128), "bf16"),
+    (3, [6, 7, 11, 1], (1, 8), "bf16"),
+    (1, [3, 0, 4], (1, 4), "f32"),
+]
+
+
+@pytest.mark.parametrize("P,lens,row_shape,dt", PAD_CASES)
+def test_padded_layout_matches_oracle(cpt, cuda_device, P, lens, row_shape, dt):
+    cu = _cu(lens)
+    T = int(cu[-1])
+    n = len(lens)
+    cup, ol2g, og2l = oracle.padded_index_map(P, cu)
+    Tpad = int(cup[-1])
+    plan = cpt.cpt_plan_create(PADDED, P, cu, T)
+    assert cpt.cpt_plan_padded_tokens(plan) == Tpad and plan.local_tokens == Tpad // P
+
+    # maps and metadata over the padded boundaries, real-token counts
+    l2g = torch.empty(Tpad, dtype=torch.int32, device="cuda")
+    g2l = torch.empty(Tpad, dtype=torch.int32, device="cuda")
+    cpt.cpt_index_map(plan, l2g, g2l)
+    ns = torch.empty(P, dtype=torch.int32, device="cuda")
+    first = torch.empty(P, dtype=torch.int32, device="cuda")
+    cul = torch.empty((P, n + 1), dtype=torch.int32, device="cuda")
+    offs = torch.empty(P + 1, dtype=torch.int32, device="cuda")
+    cpt.cpt_thd_metadata(plan, ns, first, cul, offs)
+    rl = torch.full((P, n), -1, dtype=torch.int32, device="cuda")
+    cpt.cpt_thd_real_lengths(plan, rl)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(l2g), ol2g) and np.array_equal(to_host(g2l), og2l)
+    for got, want in zip((ns, first, cul, offs), oracle.thd_metadata(DSC, P, cup, Tpad)):
+        assert np.array_equal(to_host(got), want)
+    assert np.array_equal(to_host(rl), oracle.real_lengths(DSC, P, cu, padded=True))
+
+    # partition pads on the fly, restore drops the padding
+    rng = np.random.default_rng(P + 70)
+    xs = [_rand_rows(rng, T, row_shape, dt) for _ in range(3)]
+    src = [to_dev(x) for x in xs]
+    dst = [Guarded((P, Tpad // P) + row_shape, src[0].dtype) for _ in range(3)]
+    for d in dst:
+        d.t.fill_(7.0)  # padding rows must come back as zeros
+    cpt.cpt_partition(plan, src, [d.t for d in dst])
+    back = [Guarded((T,) + row_shape, src[0].dtype) for _ in range(3)]
+    cpt.cpt_restore(plan, [d.t for d in dst], [b.t for b in back])
+    torch.cuda.synchronize()
+    for x, d, b in zip(xs, dst, back):
+        want = oracle.partition_padded(P, cu, x).reshape((P, Tpad // P) + row_shape)
+        assert np.array_equal(bits(to_host(d.t)), bits(want))
+        assert np.array_equal(bits(to_host(b.t)), bits(x))
+        assert d.bands_intact() and b.bands_intact()
+
+    # gradient return over the padded global buffer
+    wk = _writers(rng, P, Tpad, row_shape, dt)
+    ok = [Guarded((Tpad // P,) + row_shape, src[0].dtype) for _ in range(P)]
+    cpt.cpt_grad_return(plan, [to_dev(w) for w in wk], None, [o.t for o in ok], None)
+    torch.cuda.synchronize()
+    want = oracle.grad_return(ol2g, wk, oracle.F32 if dt == "f32" else oracle.BF16)
+    for o in range(P):
+        assert np.array_equal(bits(to_host(ok[o].t)), bits(want[o]))
+        assert ok[o].bands_intact()
+
+
+@pytest.mark.parametrize("layout,P,lens", [(DSC, 4, [8 * 3, 8 * 500, 0, 8 * 211]),
+                                           (PACKED, 3, [7, 1000, 3, 2590]),
+                                           (PACKED, 8, [1, 5, 0, 90, 24])])
+def test_real_lengths_unpadded(cpt, cuda_device, layout, P, lens):
+    cu = _cu(lens)
+    T = int(cu[-1])
+    plan = cpt.cpt_plan_create(layout, P, cu, T)
+    rl = torch.full((P, len(lens)), -1, dtype=torch.int32, device="cuda")
+    cpt.cpt_thd_real_lengths(plan, rl)
+    torch.cuda.synchronize()
+    want = oracle.real_lengths(layout, P, cu)
+    assert np.array_equal(to_host(rl), want)
+    assert np.array_equal(want.sum(axis=0), np.diff(cu))

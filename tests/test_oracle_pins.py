@@ -400,3 +400,58 @@ def test_grad_return_accumulate_closed_forms(oracle_lib):
     ws = [np.full((12, 4), v, np.float32) for v in (1.0, -big, 1.0)]
     out = o.grad_return_accumulate(l2g, ws, [np.full((4, 4), big, np.float32) for _ in range(P)])
     assert all(np.all(x == 1.0) for x in out)
+
+
+# ---------------------------------------------------------------- padded layout
+
+
+def _real_len_closed_form(P, lens):
+    """Real tokens of each document on each rank: the rank's chunks r and
+    2P-1-r of the padded document, each clipped to the real length."""
+    out = np.zeros((P, len(lens)), np.int64)
+    for i, L in enumerate(lens):
+        Lp = -(-L // (2 * P)) * (2 * P)
+        mp = Lp // (2 * P)
+        for r in range(P):
+            for k in (r, 2 * P - 1 - r):
+                out[r, i] += min(max(L - k * mp, 0), mp)
+    return out
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8])
+def test_padded_layout_pins(oracle_lib, P):
+    o = oracle_lib
+    rng = np.random.default_rng(50 + P)
+    for _ in range(15):
+        lens = rng.integers(0, 40, size=int(rng.integers(1, 7))).tolist()
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        T = int(cu[-1])
+        cup = o.pad_cu(P, cu)
+        Lp = np.diff(cup)
+        assert np.all(Lp % (2 * P) == 0) and np.all(Lp >= np.diff(cu)) and np.all(Lp - np.diff(cu) < 2 * P)
+        # row ids + 1 as payload: zero marks padding
+        ids = (np.arange(T, dtype=np.uint16) + 1)[:, None].repeat(4, axis=1)
+        local = o.partition_padded(P, cu, ids)
+        assert local.shape[0] == int(cup[-1])
+        nz = local[:, 0][local[:, 0] != 0]
+        assert sorted(nz.tolist()) == list(range(1, T + 1))          # each raw row exactly once
+        assert np.all(local[local[:, 0] == 0] == 0)                    # padding rows all zero
+        assert np.array_equal(o.restore_padded(P, cu, local), ids)     # un-pad inverts
+        rl = o.real_lengths(0, P, cu, padded=True)
+        assert np.array_equal(rl, _real_len_closed_form(P, lens))
+        assert np.array_equal(rl.sum(axis=0), np.diff(cu))
+        Tp = int(cup[-1]) // P
+        for r in range(P):
+            assert rl[r].sum() == np.count_nonzero(local[r * Tp:(r + 1) * Tp, 0])
+
+
+def test_padded_layout_reduces_to_plain_when_divisible(oracle_lib):
+    o = oracle_lib
+    P, cu = 4, [0, 16, 16, 48, 96]
+    assert np.array_equal(o.pad_cu(P, cu), np.array(cu, np.int32))
+    rng = np.random.default_rng(4)
+    x = rng.integers(0, 2**16, size=(96, 8), dtype=np.uint16)
+    l2g, _ = o.index_map(0, P, cu, 96)
+    assert np.array_equal(o.partition_padded(P, cu, x), o.partition(l2g, x))
+    assert np.array_equal(o.real_lengths(0, P, cu, padded=True), o.real_lengths(0, P, cu))
+    assert np.array_equal(o.real_lengths(0, P, cu), np.tile(np.diff(cu) // P, (P, 1)))

@@ -92,3 +92,19 @@ def test_noalloc_rejects_batches_beyond_its_limit(cpt, cuda_device):
     assert "no-allocation limit" in str(ei.value)
     torch.cuda.synchronize()
     assert bool((o == 3.0).all().item())
+
+
+def test_noalloc_padded_layout_matches_plan_path(cpt, cuda_device):
+    P, lens = 4, [13, 0, 1000, 7]
+    cu = synth.cu_from_lengths(lens)
+    T = int(cu[-1])
+    plan = cpt.cpt_plan_create(cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED, P, cu, T)
+    Tpad = plan.padded_tokens
+    rng = np.random.default_rng(5)
+    w = torch.stack([to_dev(synth.normal_bf16(rng, (Tpad, 2, 64))) for _ in range(P)])
+    a = torch.empty((P, Tpad // P, 2, 64), dtype=torch.bfloat16, device="cuda")
+    b = torch.empty_like(a)
+    cpt.cpt_grad_return_noalloc(cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED, P, cu, T, w, None, a, None)
+    cpt.cpt_grad_return(plan, w, None, b, None)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
