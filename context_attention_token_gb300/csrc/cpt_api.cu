@@ -55,6 +55,23 @@ cpt_status cuda_fail(cudaError_t e, const char *what)
     return fail(CPT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Calls whose work depends on host state at the time of the call (a plan's
+// host-to-device copy of cu_seqlens, the epoch bookkeeping) cannot be
+// recorded into a CUDA graph: a replay would reuse stale host decisions.
+cpt_status refuse_capture(void *stream, const char *what)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail(e, "cudaStreamIsCapturing");
+    }
+    if (cs != cudaStreamCaptureStatusNone)
+        return fail(CPT_ERR_UNSUPPORTED, "%s cannot be recorded into a CUDA graph: call it outside "
+                    "stream capture", what);
+    return CPT_OK;
+}
+
 int current_device(int *dev)
 {
     return cudaGetDevice(dev) == cudaSuccess;
@@ -344,6 +361,7 @@ cpt_status cpt_plan_create(cpt_layout layout, int32_t P, const int32_t *cu, int3
     if (st) return st;
     int dev = 0;
     if (!current_device(&dev)) return fail(CPT_ERR_CUDA, "cudaGetDevice failed");
+    if ((st = refuse_capture(stream, "cpt_plan_create"))) return st;
     const WsLayout w = ws_layout(layout, P, n, T);
     if (workspace == nullptr) return fail(CPT_ERR_WORKSPACE, "workspace is NULL");
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
@@ -841,6 +859,7 @@ cpt_status cpt_epoch_publish(cpt_epoch *ep, int32_t writer, void *stream)
     if (st) return st;
     if (writer < 0 || writer >= ep->P)
         return fail(CPT_ERR_INVALID_ARG, "writer %d outside 0..%d", writer, ep->P - 1);
+    if ((st = refuse_capture(stream, "cpt_epoch_publish"))) return st;
     std::lock_guard<std::mutex> lock(ep->mu);
     if (ep->epoch == 0) return fail(CPT_ERR_INVALID_ARG, "no epoch started (call cpt_epoch_advance)");
     const DriverOps &d = driver_ops();
@@ -869,6 +888,7 @@ cpt_status cpt_epoch_wait(cpt_epoch *ep, int32_t owner, uint64_t timeout_ns, cpt
         return fail(CPT_ERR_INVALID_ARG, "unknown wait mode %d", (int)mode);
     if (timeout_ns > 10ull * 1000 * 1000 * 1000)
         return fail(CPT_ERR_INVALID_ARG, "timeout_ns above 10 s");
+    if ((st = refuse_capture(stream, "cpt_epoch_wait"))) return st;
     std::lock_guard<std::mutex> lock(ep->mu);
     if (ep->epoch == 0) return fail(CPT_ERR_INVALID_ARG, "no epoch started (call cpt_epoch_advance)");
     const DriverOps &d = driver_ops();

@@ -120,3 +120,40 @@ def test_partition_pages_shape_sampled(cpt, big_plan):
         assert torch.equal(b.view(torch.int16), x.view(torch.int16))
     del qkv, dst, back
     torch.cuda.empty_cache()
+
+
+def test_largest_batch_the_maps_allow(cpt, cuda_device):
+    """T = 2^31 - 8 tokens (one document, P=4, 16-byte rows): the int32 maps
+    and every 64-bit offset in the kernels at their limit."""
+    T, Pm = 2**31 - 8, 4
+    m = T // (2 * Pm)
+    Tp = T // Pm
+    plan = cpt.cpt_plan_create(0, Pm, [0, T], T)
+    l2g = torch.empty(T, dtype=torch.int32, device="cuda")
+    g2l = torch.empty(T, dtype=torch.int32, device="cuda")
+    cpt.cpt_index_map(plan, l2g, g2l)
+    torch.cuda.synchronize()
+    # the ownership rule: rank r holds chunk r, then chunk 2P-1-r
+    for r in range(Pm):
+        for j in (0, 1, m - 1, m, m + 1, Tp - 1):
+            want = r * m + j if j < m else (2 * Pm - 1 - r) * m + (j - m)
+            assert int(l2g[r * Tp + j].item()) == want
+    step = 1 << 27
+    for a in range(0, T, step):
+        b = min(a + step, T)
+        idx = l2g[a:b].long()
+        assert torch.equal(g2l[idx].long(), torch.arange(a, b, device="cuda"))
+    del g2l, idx
+    # row-id payload: global row g holds g in all four words; after the
+    # partition local row q must hold l2g[q]
+    src = torch.arange(T, dtype=torch.int32, device="cuda").view(T, 1).expand(T, 4).contiguous()
+    dst = torch.empty((Pm, Tp, 4), dtype=torch.int32, device="cuda")
+    cpt.cpt_partition(plan, [src.view(torch.float32)], [dst.view(torch.float32)])
+    torch.cuda.synchronize()
+    flat = dst.view(T, 4)
+    for a in range(0, T, step):
+        b = min(a + step, T)
+        blk = flat[a:b]
+        assert torch.equal(blk[:, 0], l2g[a:b]) and bool((blk == blk[:, :1]).all().item())
+    del src, dst, flat, l2g
+    torch.cuda.empty_cache()
