@@ -417,29 +417,52 @@ def run_gpu(args):
         h_qkv, h_dkw, h_dvw = host_in[:3], host_in[3], host_in[4]
         h_part, h_dko, h_dvo = host_out[:3], host_out[3], host_out[4]
 
+        # Each global chunk of the DualChunkSwap map (2P chunks of m tokens)
+        # feeds one contiguous range of local rows; read the map back once
+        # (outside the timed region) to find those ranges.
+        m = S // (2 * P)
+        probe = cpt.cpt_plan_create(cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP, P, cu, S, workspace=ws)
+        g2l_dev = torch.empty(S, dtype=torch.int32, device=dev)
+        l2g_dev = torch.empty(S, dtype=torch.int32, device=dev)
+        cpt.cpt_index_map(probe, l2g_dev, g2l_dev)
+        g2l = g2l_dev.cpu()
+        chunks = []
+        for k in range(2 * P):
+            qs = g2l[k * m:(k + 1) * m]
+            q0 = int(qs[0])
+            if not bool((qs == torch.arange(q0, q0 + m, dtype=qs.dtype)).all()):
+                raise RuntimeError("chunk of the map is not a contiguous local range")
+            chunks.append((k * m, q0))
+        del probe, g2l_dev, l2g_dev
+        flat = lambda t: t.view(S, H, D)  # noqa: E731  rank-major local tensor as [S, H, D]
+
         def e2e_step():
-            # Two independent chains on two streams, so one chain's copies
-            # overlap the other's: Q/K/V in -> plan -> partition -> parts out
-            # on the main stream; dK/dV in -> grad_return (after the plan) ->
-            # owner gradients out on the side stream.
-            side.wait_stream(stream)
-            with torch.cuda.stream(side):
-                dkw.copy_(h_dkw, non_blocking=True)
-                dvw.copy_(h_dvw, non_blocking=True)
-            for d, h in zip(qkv, h_qkv):
-                d.copy_(h, non_blocking=True)
+            # Two independent chains on two streams, each pipelined over the 2P
+            # global chunks: chunk k's host-to-device copies overlap the
+            # kernels and device-to-host copies of chunk k-1.
+            #   main: Q/K/V rows in -> partition of their local rows -> out
+            #   side: dK/dV rows of every writer in -> grad_return of their
+            #         local rows -> owner rows out
             plan = cpt.cpt_plan_create(cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP, P, cu, S, workspace=ws)
             plan_ready = torch.cuda.Event()
             plan_ready.record(stream)
-            cpt.cpt_partition(plan, qkv, part)
-            for h, d in zip(h_part, part):
-                h.copy_(d, non_blocking=True)
             side.wait_event(plan_ready)
-            cpt.cpt_grad_return(plan, dkw, dvw, dko, dvo, stream=side)
-            with torch.cuda.stream(side):
-                h_dko.copy_(dko, non_blocking=True)
-                h_dvo.copy_(dvo, non_blocking=True)
+            for g0, q0 in chunks:
+                for d, h in zip(qkv, h_qkv):
+                    d[g0:g0 + m].copy_(h[g0:g0 + m], non_blocking=True)
+                cpt.cpt_partition_rows(plan, qkv, part, q0, m)
+                for h, d in zip(h_part, part):
+                    flat(h)[q0:q0 + m].copy_(flat(d)[q0:q0 + m], non_blocking=True)
+                with torch.cuda.stream(side):
+                    for w in range(P):
+                        dkw[w, g0:g0 + m].copy_(h_dkw[w, g0:g0 + m], non_blocking=True)
+                        dvw[w, g0:g0 + m].copy_(h_dvw[w, g0:g0 + m], non_blocking=True)
+                cpt.cpt_grad_return_rows(plan, dkw, dvw, dko, dvo, q0, m, stream=side)
+                with torch.cuda.stream(side):
+                    flat(h_dko)[q0:q0 + m].copy_(flat(dko)[q0:q0 + m], non_blocking=True)
+                    flat(h_dvo)[q0:q0 + m].copy_(flat(dvo)[q0:q0 + m], non_blocking=True)
             stream.wait_stream(side)
+            side.wait_stream(stream)
             cpt.cpt_plan_destroy(plan)
 
         e2e_steps = max(1, min(args.steps, args.e2e_steps))

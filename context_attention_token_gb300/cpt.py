@@ -81,6 +81,9 @@ _sig("cpt_thd_metadata", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("cpt_partition", ctypes.c_int, _vp, _i32, _vp, _vp, _i64, ctypes.c_int, _vp)
 _sig("cpt_grad_return_accumulate", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, ctypes.c_int,
      ctypes.c_int, _vp)
+_sig("cpt_partition_rows", ctypes.c_int, _vp, _i32, _vp, _vp, _i64, ctypes.c_int, _i64, _i64, _vp)
+_sig("cpt_grad_return_rows", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, ctypes.c_int, ctypes.c_int,
+     _i64, _i64, _vp)
 _sig("cpt_restore", ctypes.c_int, _vp, _i32, _vp, _vp, _i64, ctypes.c_int, _vp)
 _sig("cpt_grad_return", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, ctypes.c_int, ctypes.c_int, _vp)
 _sig("cpt_grad_return_noalloc", ctypes.c_int, ctypes.c_int, _i32, _vp, _i32, _i64, _vp, _vp, _vp, _vp,
@@ -307,6 +310,16 @@ def cpt_partition(plan: Plan, srcs, dsts, stream=None):
                               _stream(stream)))
 
 
+def cpt_partition_rows(plan: Plan, srcs, dsts, local_begin: int, local_count: int, stream=None):
+    """cpt_partition for flattened local rows [local_begin, local_begin + local_count) only."""
+    srcs, dsts = list(srcs), list(dsts)
+    if len(srcs) != len(dsts):
+        raise ValueError("srcs and dsts differ in length")
+    _check(_lib.cpt_partition_rows(plan.handle, len(srcs), ctypes.cast(_ptr_array(srcs), _vp),
+                                   ctypes.cast(_ptr_array(dsts), _vp), _row_elems(srcs[0]),
+                                   _dtype_code(srcs[0]), local_begin, local_count, _stream(stream)))
+
+
 def cpt_restore(plan: Plan, srcs, dsts, stream=None):
     """dsts[t] ([T, ...]) = global-order copy of the rank-local srcs[t] ([P, T/P, ...])."""
     srcs, dsts = list(srcs), list(dsts)
@@ -343,6 +356,20 @@ def cpt_grad_return(plan: Plan, dk_writers, dv_writers, dk_owners, dv_owners, st
     the dV pair may be None.
     """
     _grad_return(_lib.cpt_grad_return, plan, dk_writers, dv_writers, dk_owners, dv_owners, stream)
+
+
+def cpt_grad_return_rows(plan: Plan, dk_writers, dv_writers, dk_owners, dv_owners,
+                         local_begin: int, local_count: int, stream=None):
+    """cpt_grad_return for flattened owner-major local rows [local_begin, +local_count) only."""
+    P = plan.cp_size
+    dkw = _Parts(dk_writers, P)
+    dko = _Parts(dk_owners, P)
+    dvw = _Parts(dv_writers, P) if dv_writers is not None else None
+    dvo = _Parts(dv_owners, P) if dv_owners is not None else None
+    _check(_lib.cpt_grad_return_rows(
+        plan.handle, dkw.array(), dvw.array() if dvw is not None else None, dko.array(),
+        dvo.array() if dvo is not None else None, dkw.row_elems(), dkw.code(), dko.code(),
+        local_begin, local_count, _stream(stream)))
 
 
 def cpt_grad_return_accumulate(plan: Plan, dk_writers, dv_writers, dk_owners, dv_owners,

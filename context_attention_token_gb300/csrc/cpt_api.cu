@@ -531,19 +531,29 @@ static cpt_status check_row(int64_t row_elems, cpt_dtype a, cpt_dtype b, int64_t
     return CPT_OK;
 }
 
-cpt_status cpt_partition(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
-                         void *const *dst, int64_t row_elems, cpt_dtype dtype, void *stream)
+// Local rows [begin, begin + count) of a plan, flattened rank-major.
+static cpt_status check_local_range(const cpt_plan *plan, int64_t begin, int64_t count)
 {
-    Trace trace("cpt_partition");
+    if (begin < 0 || count < 0 || begin > plan->Tpad || count > plan->Tpad - begin)
+        return fail(CPT_ERR_INVALID_ARG, "local rows [%lld, %lld) outside [0, %lld)",
+                    (long long)begin, (long long)(begin + count), (long long)plan->Tpad);
+    return CPT_OK;
+}
+
+static cpt_status partition_impl(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
+                                 void *const *dst, int64_t row_elems, cpt_dtype dtype,
+                                 int64_t begin, int64_t count, void *stream)
+{
     int dev = 0;
     cpt_status st = check_plan(plan, &dev);
     if (st) return st;
+    if ((st = check_local_range(plan, begin, count))) return st;
     if (n_tensors < 1 || n_tensors > kMaxTensors)
         return fail(CPT_ERR_INVALID_ARG, "n_tensors %d outside 1..3", n_tensors);
     if (src == nullptr || dst == nullptr) return fail(CPT_ERR_INVALID_ARG, "src or dst is NULL");
     int64_t units = 0;
     if ((st = check_row(row_elems, dtype, dtype, &units))) return st;
-    if (plan->Tpad == 0) return CPT_OK;
+    if (count == 0) return CPT_OK;
     const int64_t row_bytes = units * 16;
     std::vector<Range> r;
     add_range(r, plan->ws, plan->ws_bytes, false, "workspace");
@@ -565,13 +575,31 @@ cpt_status cpt_partition(const cpt_plan *plan, int32_t n_tensors, const void *co
         for (int o = 0; o < plan->P; ++o)
             p.dst[t][o] = static_cast<uint8_t *>(dst[t]) + (int64_t)o * plan->Tp * row_bytes;
     }
-    p.T = plan->Tpad;
+    p.q0 = begin;
+    p.T = count;
     p.Tp = plan->Tp;
-    p.rows = (int64_t)n_tensors * plan->Tpad;
+    p.rows = (int64_t)n_tensors * count;
     p.units = (int32_t)units;
     p.row_bytes = (int32_t)row_bytes;
     cudaError_t e = launch_gather(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CPT_OK : cuda_fail(e, "partition launch");
+}
+
+cpt_status cpt_partition(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
+                         void *const *dst, int64_t row_elems, cpt_dtype dtype, void *stream)
+{
+    Trace trace("cpt_partition");
+    if (plan == nullptr) return fail(CPT_ERR_INVALID_ARG, "plan is NULL");
+    return partition_impl(plan, n_tensors, src, dst, row_elems, dtype, 0, plan->Tpad, stream);
+}
+
+cpt_status cpt_partition_rows(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
+                              void *const *dst, int64_t row_elems, cpt_dtype dtype,
+                              int64_t local_begin, int64_t local_count, void *stream)
+{
+    Trace trace("cpt_partition_rows");
+    return partition_impl(plan, n_tensors, src, dst, row_elems, dtype, local_begin, local_count,
+                          stream);
 }
 
 cpt_status cpt_restore(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
@@ -629,18 +657,19 @@ cpt_status cpt_restore(const cpt_plan *plan, int32_t n_tensors, const void *cons
 static cpt_status grad_return_impl(const cpt_plan *plan, const void *const *dkw,
                                    const void *const *dvw, void *const *dko, void *const *dvo,
                                    int64_t row_elems, cpt_dtype in, cpt_dtype out, void *stream,
-                                   bool accumulate)
+                                   bool accumulate, int64_t begin, int64_t count)
 {
     int dev = 0;
     cpt_status st = check_plan(plan, &dev);
     if (st) return st;
+    if ((st = check_local_range(plan, begin, count))) return st;
     if (dkw == nullptr || dko == nullptr)
         return fail(CPT_ERR_INVALID_ARG, "dk_writers or dk_owners is NULL");
     if ((dvw == nullptr) != (dvo == nullptr))
         return fail(CPT_ERR_INVALID_ARG, "dv_writers and dv_owners must both be given or both NULL");
     int64_t units = 0;
     if ((st = check_row(row_elems, in, out, &units))) return st;
-    if (plan->Tpad == 0) return CPT_OK;
+    if (count == 0) return CPT_OK;
     const int nt = dvw ? 2 : 1;
     const int P = plan->P;
     const int64_t in_row = units * 16;
@@ -669,9 +698,10 @@ static cpt_status grad_return_impl(const cpt_plan *plan, const void *const *dkw,
             p.w[t][w] = static_cast<const uint8_t *>(W[t][w]);
             p.o[t][w] = static_cast<uint8_t *>(O[t][w]);
         }
-    p.T = plan->Tpad;
+    p.q0 = begin;
+    p.T = count;
     p.Tp = plan->Tp;
-    p.rows = (int64_t)nt * plan->Tpad;
+    p.rows = (int64_t)nt * count;
     p.units = (int32_t)units;
     p.in_row_bytes = (int32_t)in_row;
     p.out_row_bytes = (int32_t)out_row;
@@ -685,7 +715,9 @@ cpt_status cpt_grad_return(const cpt_plan *plan, const void *const *dkw, const v
                            cpt_dtype out, void *stream)
 {
     Trace trace("cpt_grad_return");
-    return grad_return_impl(plan, dkw, dvw, dko, dvo, row_elems, in, out, stream, false);
+    if (plan == nullptr) return fail(CPT_ERR_INVALID_ARG, "plan is NULL");
+    return grad_return_impl(plan, dkw, dvw, dko, dvo, row_elems, in, out, stream, false, 0,
+                            plan->Tpad);
 }
 
 cpt_status cpt_grad_return_accumulate(const cpt_plan *plan, const void *const *dkw,
@@ -693,7 +725,19 @@ cpt_status cpt_grad_return_accumulate(const cpt_plan *plan, const void *const *d
                                       int64_t row_elems, cpt_dtype in, cpt_dtype out, void *stream)
 {
     Trace trace("cpt_grad_return_accumulate");
-    return grad_return_impl(plan, dkw, dvw, dko, dvo, row_elems, in, out, stream, true);
+    if (plan == nullptr) return fail(CPT_ERR_INVALID_ARG, "plan is NULL");
+    return grad_return_impl(plan, dkw, dvw, dko, dvo, row_elems, in, out, stream, true, 0,
+                            plan->Tpad);
+}
+
+cpt_status cpt_grad_return_rows(const cpt_plan *plan, const void *const *dkw,
+                                const void *const *dvw, void *const *dko, void *const *dvo,
+                                int64_t row_elems, cpt_dtype in, cpt_dtype out, int64_t local_begin,
+                                int64_t local_count, void *stream)
+{
+    Trace trace("cpt_grad_return_rows");
+    return grad_return_impl(plan, dkw, dvw, dko, dvo, row_elems, in, out, stream, false,
+                            local_begin, local_count);
 }
 
 cpt_status cpt_grad_scatter(const cpt_plan *plan, int32_t writer, const void *src,

@@ -45,8 +45,9 @@ struct GatherParams {
     const int32_t *l2g;                  // nullptr: identity map
     const uint8_t *src[kMaxTensors];     // [T][row_bytes]
     uint8_t *dst[kMaxTensors][kMaxCp];   // per tensor, per rank: [Tp][row_bytes]
-    int64_t T;
-    int64_t Tp;
+    int64_t q0;          // first output row of the launch (flattened)
+    int64_t T;           // output rows per tensor in the launch
+    int64_t Tp;          // output rows per rank piece
     int64_t rows;        // n_tensors * T
     int32_t units;       // 16-byte units per row
     int32_t row_bytes;
@@ -59,8 +60,9 @@ struct GradReturnParams {
     const int32_t *l2g;              // [T]
     const uint8_t *w[2][kMaxCp];     // writer w's global gradient [T][in_row_bytes]
     uint8_t *o[2][kMaxCp];           // owner o's local gradient [Tp][out_row_bytes]
-    int64_t T;
-    int64_t Tp;
+    int64_t q0;            // first local row of the launch (flattened owner-major)
+    int64_t T;             // local rows per tensor in the launch
+    int64_t Tp;            // local rows per owner
     int64_t rows;          // n_tensors * T
     int32_t units;         // 16-byte input units per row
     int32_t in_row_bytes;

@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p)
 
     for (int64_t R = warp; R < p.rows; R += nwarps) {
         const int t = (R >= p.T) + (R >= 2 * p.T);
-        const int64_t q = R - t * p.T;
+        const int64_t q = p.q0 + (R - t * p.T);
         const int r = (int)(q / p.Tp);
         const int64_t j = q - (int64_t)r * p.Tp;
         const int64_t g = p.l2g ? (int64_t)__ldg(p.l2g + q) : q;

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) grad_return_kernel(const GradReturnP
 
     for (int64_t R = warp; R < p.rows; R += nwarps) {
         const int t = R >= p.T;
-        const int64_t q = R - t * p.T;
+        const int64_t q = p.q0 + (R - t * p.T);
         const int o = (int)(q / p.Tp);
         const int64_t j = q - (int64_t)o * p.Tp;
         const int64_t g = __ldg(p.l2g + q);

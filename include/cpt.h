@@ -281,6 +281,17 @@ CPT_API cpt_status cpt_thd_real_lengths(const cpt_plan *plan, int32_t *real_len,
 CPT_API cpt_status cpt_partition(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
                          void *const *dst, int64_t row_elems, cpt_dtype dtype, void *stream);
 
+/* cpt_partition restricted to flattened local rows [local_begin,
+ * local_begin + local_count) of the rank-major output: only those rows are
+ * written, each from the source row the map assigns it. Lets a caller
+ * overlap host-to-device copies of one part of the batch with the reorder
+ * of another. Buffers are the full tensors of cpt_partition. Errors: those
+ * of cpt_partition; CPT_ERR_INVALID_ARG for a range outside [0, T_pad). */
+CPT_API cpt_status cpt_partition_rows(const cpt_plan *plan, int32_t n_tensors,
+                                      const void *const *src, void *const *dst, int64_t row_elems,
+                                      cpt_dtype dtype, int64_t local_begin, int64_t local_count,
+                                      void *stream);
+
 /* All-gather restore: put rank-local token tensors back into global order,
  * the inverse of cpt_partition ([TE-3221] "Scope and constraints": all-gather
  * CP; commit "Allow relaxed THD all-gather ...": rank-major ownership is the
@@ -320,6 +331,18 @@ CPT_API cpt_status cpt_grad_return(const cpt_plan *plan, const void *const *dk_w
                            const void *const *dv_writers, void *const *dk_owners,
                            void *const *dv_owners, int64_t row_elems, cpt_dtype in,
                            cpt_dtype out, void *stream);
+
+/* cpt_grad_return restricted to flattened owner-major local rows
+ * [local_begin, local_begin + local_count): only those owner rows are
+ * written, each summed from the writer rows the map assigns it, so a caller
+ * can start on the rows whose writer inputs have arrived. Buffers are the
+ * full tensors of cpt_grad_return. Errors: those of cpt_grad_return;
+ * CPT_ERR_INVALID_ARG for a range outside [0, T_pad). */
+CPT_API cpt_status cpt_grad_return_rows(const cpt_plan *plan, const void *const *dk_writers,
+                                        const void *const *dv_writers, void *const *dk_owners,
+                                        void *const *dv_owners, int64_t row_elems, cpt_dtype in,
+                                        cpt_dtype out, int64_t local_begin, int64_t local_count,
+                                        void *stream);
 
 /* As cpt_grad_return, but the owners' current gradients start the sums (the
  * other reading of "accumulates four writer slots into the local owner's

@@ -491,3 +491,45 @@ def test_real_lengths_unpadded(cpt, cuda_device, layout, P, lens):
     want = oracle.real_lengths(layout, P, cu)
     assert np.array_equal(to_host(rl), want)
     assert np.array_equal(want.sum(axis=0), np.diff(cu))
+
+
+# ---------------------------------------------------------------- row ranges
+
+
+@pytest.mark.parametrize("layout,P,lens", [(DSC, 4, [8 * 300, 0, 8 * 97]), (PACKED, 3, [7, 1000, 3, 2590]),
+                                           (PADDED, 4, [13, 0, 1000, 7])])
+def test_row_range_calls_cover_the_full_calls(cpt, cuda_device, layout, P, lens):
+    """Ragged row pieces that together cover the batch give the full result;
+    rows outside a single piece are not touched."""
+    cu = _cu(lens)
+    T = int(cu[-1])
+    row = (2, 64)
+    plan = cpt.cpt_plan_create(layout, P, cu, T)
+    Tpad = plan.padded_tokens
+    rng = np.random.default_rng(31)
+    hq = synth.normal_bf16(rng, (T,) + row)
+    hw = [synth.normal_bf16(rng, (Tpad,) + row) for _ in range(P)]
+    q = to_dev(hq)
+    w = torch.stack([to_dev(x) for x in hw])
+    full_q = torch.empty((P, Tpad // P) + row, dtype=torch.bfloat16, device="cuda")
+    full_o = torch.empty((P, Tpad // P) + row, dtype=torch.bfloat16, device="cuda")
+    cpt.cpt_partition(plan, [q], [full_q])
+    cpt.cpt_grad_return(plan, w, None, full_o, None)
+    cuts = sorted(set([0, Tpad] + rng.integers(0, Tpad, size=9).tolist()))
+    part_q = torch.full_like(full_q, 5.0)
+    part_o = torch.full_like(full_o, 5.0)
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        cpt.cpt_partition_rows(plan, [q], [part_q], a, b - a)
+        cpt.cpt_grad_return_rows(plan, w, None, part_o, None, a, b - a)
+    one_q = torch.full_like(full_q, 5.0)
+    a, b = Tpad // 3, Tpad // 3 + 101
+    cpt.cpt_partition_rows(plan, [q], [one_q], a, b - a)
+    torch.cuda.synchronize()
+    assert torch.equal(part_q.view(torch.int16), full_q.view(torch.int16))
+    assert torch.equal(part_o.view(torch.int16), full_o.view(torch.int16))
+    flat = one_q.view(Tpad, -1)
+    assert torch.equal(flat[a:b].view(torch.int16), full_q.view(Tpad, -1)[a:b].view(torch.int16))
+    assert bool((flat[:a] == 5.0).all().item()) and bool((flat[b:] == 5.0).all().item())
+    with pytest.raises(cpt.CptError) as ei:
+        cpt.cpt_grad_return_rows(plan, w, None, part_o, None, Tpad - 1, 2)
+    assert ei.value.status == cpt.CPT_ERR_INVALID_ARG
