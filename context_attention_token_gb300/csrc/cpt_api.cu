@@ -1,11 +1,12 @@
 // C ABI of the library (declared in include/cpt.h): host-side validation,
 // the plan and epoch objects, and kernel dispatch.
 //
-// Every check runs before anything is enqueued ("fail-closed validation
-// boundary", "Add stream-ordered CP gradient return primitive",
-// TransformerEngine PR 3235, author's reply): device membership of every
-// pointer ("cp_check_current_device guards on all tensor arguments", same
-// page, "Greptile Summary"), alignment, sizes, overlaps between outputs and
+// Every check runs before anything is enqueued, and unsupported input is
+// refused rather than attempted ("Add stream-ordered CP gradient return
+// primitive", TransformerEngine PR 3235, author's reply on its size check):
+// device membership of every pointer (the page's "Greptile Summary" lists a
+// current-device guard on each tensor argument), alignment, sizes, overlaps
+// between outputs and
 // every other buffer of the call, and the self-slot alias of the staged
 // scatter. The driver's stream memory operations are resolved at run time
 // through the runtime's driver entry-point query, so the library has no

@@ -36,9 +36,10 @@
  *   Streams     `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *               default stream). Every call is asynchronous on it unless
  *               stated; outputs are valid once the stream reaches the call.
- *   Errors      Checks run on the host before anything is launched
- *               ("fail-closed validation boundary", [TE-3235] author's
- *               reply). On failure nothing is enqueued, the call returns a
+ *   Errors      Checks run on the host before anything is launched, and
+ *               anything outside the supported scope is refused rather than
+ *               attempted (as the author's reply in [TE-3235] describes its
+ *               size check). On failure nothing is enqueued, the call returns a
  *               non-zero cpt_status and cpt_last_error_string() explains it.
  *               Device-side failures (epoch wait timeout) go to a device
  *               status word. Nothing aborts or traps.
@@ -87,10 +88,9 @@ typedef enum cpt_status {
 
 /* Token ownership policy ([TE-3221] "Why").
  *  DUAL_CHUNK_SWAP    per document: every document is cut into 2P equal
- *                     chunks; rank r owns chunks r and 2P-1-r ([TE-3235]
- *                     author's reply: "owner o receives native sequence
- *                     chunks o and (2*N-1-o)"), kept in ascending global
- *                     position, documents in order. Each document length
+ *                     chunks; rank r owns chunks r and 2P-1-r (the owner
+ *                     rule of [TE-3235], author's reply), kept in ascending
+ *                     global position, documents in order. Each document length
  *                     must divide by 2P.
  *  PACKED_CONTIGUOUS  the whole packed buffer is cut into P equal contiguous
  *                     chunks, rank r owning the r-th; document boundaries
@@ -276,6 +276,10 @@ CPT_API cpt_status cpt_thd_real_lengths(const cpt_plan *plan, int32_t *real_len,
  *             dst. Padding rows of the padded layout are written as zeros.
  *  row_elems  elements per token row (H*D); row bytes must be a multiple
  *             of 16.
+ *  For PACKED_CONTIGUOUS the map is the identity: src viewed as [P][T/P][row]
+ *  already is the rank-local layout (rank-major ownership requires no K/V
+ *  reorder), so a caller may use that view instead; this call then performs
+ *  a plain copy.
  *  Errors: CPT_ERR_INVALID_ARG, CPT_ERR_DEVICE, CPT_ERR_ALIGNMENT,
  *  CPT_ERR_ALIAS, CPT_ERR_CUDA. */
 CPT_API cpt_status cpt_partition(const cpt_plan *plan, int32_t n_tensors, const void *const *src,
@@ -294,8 +298,8 @@ CPT_API cpt_status cpt_partition_rows(const cpt_plan *plan, int32_t n_tensors,
 
 /* All-gather restore: put rank-local token tensors back into global order,
  * the inverse of cpt_partition ([TE-3221] "Scope and constraints": all-gather
- * CP; commit "Allow relaxed THD all-gather ...": rank-major ownership is the
- * policy that needs no KV reorder, so the per-document one does):
+ * CP; commit "Allow relaxed THD all-gather ...": only rank-major ownership
+ * leaves K and V in global order, so the per-document policy must reorder):
  *   dst[t][g] = src[t][g2l[g]], i.e. dst[t][l2g[q]] = src[t][q], a bit copy.
  *  src        host array of n_tensors device pointers, each [P][T_pad/P][row]
  *             (the all-gathered rank-major buffer).
@@ -345,8 +349,8 @@ CPT_API cpt_status cpt_grad_return_rows(const cpt_plan *plan, const void *const 
                                         void *stream);
 
 /* As cpt_grad_return, but the owners' current gradients start the sums (the
- * other reading of "accumulates four writer slots into the local owner's
- * dK/dV", [TE-3235] "Description"):
+ * other reading of the accumulation step in [TE-3235] "Description", where
+ * the owner adds its writer slots into its gradient):
  *   out[o][j] = round((((out[o][j] + x_0) + x_1) + ...) + x_{P-1}),
  * the existing owner value widened exactly to binary32 first. Each owner row
  * is read once more than in cpt_grad_return. Arguments and errors: as
@@ -399,8 +403,8 @@ CPT_API cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t cp_size,
 /* ------------------------------------------------------------------ */
 
 /* Scatter one writer's global gradient into its slot of every owner
- * ([TE-3235] sequence diagram, "copy_() scatter dk_global to
- * peer_grad_key_returns[owner][rank]"): slots[o][j] = src[l2g[o*T/P + j]].
+ * ([TE-3235] sequence diagram: each rank copies its global dK into its slot
+ * of every owner's peer_grad_key_returns): slots[o][j] = src[l2g[o*T/P + j]].
  *  writer     0..P-1.
  *  src        device [T][row].
  *  slots      host array of P device pointers: slots[o] is this writer's
@@ -443,8 +447,9 @@ CPT_API cpt_status cpt_epoch_advance(cpt_epoch *ep, uint32_t *epoch_out);
 CPT_API cpt_status cpt_epoch_publish(cpt_epoch *ep, int32_t writer, void *stream);
 
 /* Make `stream` wait until every writer has published the current epoch to
- * `owner` ([TE-3235] sequence diagram: wait until all cp_size slots are
- * >= epoch; the comparison is wrap-around safe, (int32)(flag - epoch) >= 0).
+ * `owner` ([TE-3235] sequence diagram: the owner waits for every one of its
+ * cp_size epoch slots to reach the epoch; here the comparison is wrap-around
+ * safe, (int32)(flag - epoch) >= 0).
  *  Host check first: if some writer has not yet enqueued its publish of this
  *  epoch, nothing waits; status[owner] is set to CPT_ERR_NOT_PUBLISHED on
  *  `stream` and the call returns CPT_ERR_NOT_PUBLISHED.
@@ -469,8 +474,8 @@ CPT_API cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *st
 /* ------------------------------------------------------------------ */
 
 /* One-shot ordered sum of n_slots equally sized buffers ([TE-3235]
- * sequence diagram "accumulate grad_key_return[0..cp_size-1]"; [NVSHMEM]
- * one-shot all-reduce, every element reading all slots in one step):
+ * sequence diagram, where each owner sums its return slots 0..cp_size-1;
+ * [NVSHMEM] one-shot all-reduce, every element reading all slots in one step):
  *   dst[i] = round(((s_0[i] + s_1[i]) + ...) + s_{n-1}[i]) in binary32.
  *  slots     host array of n_slots (1..8) device pointers, each n_elems
  *            elements of type `in`.

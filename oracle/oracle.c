@@ -75,7 +75,7 @@ static int dsc_owner_of_chunk(int k, int P)
 /* DSC ([TE-3221] "Why", [TE-3235] reply): every document i of length  */
 /* L_i is cut into 2P chunks of m_i = L_i/(2P) tokens. Rank r takes    */
 /* its chunks in ascending global position, document by document       */
-/* (the "native two-chunk CP layout" of [TE-3235] "Description").      */
+/* (the two-chunk CP layout named in [TE-3235] "Description").         */
 /* Written as an explicit walk over every chunk of every document.     */
 /*                                                                     */
 /* Packed-contiguous ([TE-3221] commit "Allow relaxed THD all-gather   */
@@ -125,9 +125,9 @@ int oracle_index_map(int layout, int P, const int32_t *cu, int n, int64_t T,
 /* every rank has all n documents as segments and cu_local = cu/P.     */
 /*                                                                     */
 /* Packed ([TE-3221] commit "Keep per-document partitioning as the     */
-/* default ...": one chunk and one attention step per rank, document   */
-/* isolation kept through sequence metadata): rank r's chunk is        */
-/* [a,b) = [r*T/P, (r+1)*T/P). Its segments are the non-empty          */
+/* default ...": each rank holds a single chunk and runs a single      */
+/* attention step; the metadata keeps documents apart): rank r's      */
+/* chunk is [a,b) = [r*T/P, (r+1)*T/P). Its segments are the non-empty */
 /* intersections [cu_i, cu_{i+1}) with [a,b), in document order;       */
 /* cu_local lists their starts relative to a, then b-a. Entries past   */
 /* num_segs[r] repeat T/P. seg_doc_first[r] is the first document that */
@@ -192,7 +192,7 @@ void oracle_partition(const int32_t *l2g, int64_t T, const void *src, void *dst,
 /* every rank holds the rank-major buffer [P][T/P][row]; the per-      */
 /* document layout must be put back into global token order before    */
 /* attention sees it ([TE-3221] commit "Allow relaxed THD all-gather   */
-/* ...": rank-major ownership is the case that needs no KV reorder).   */
+/* ...": only rank-major ownership leaves K and V in global order).    */
 /* Written as the definition: local row q goes to global row l2g[q].   */
 /* Parity: pinned (round trip with the partition, brute-force map).    */
 /* ------------------------------------------------------------------ */
@@ -327,8 +327,8 @@ static void store_elem(void *base, int dtype, int64_t idx, float v)
 }
 
 /* ------------------------------------------------------------------ */
-/* Ordered sum of P slot buffers ([TE-3235] sequence diagram:          */
-/* "accumulate grad_key_return[0..cp_size-1]"; the one-shot sum of     */
+/* Ordered sum of P slot buffers ([TE-3235] sequence diagram: each     */
+/* owner sums its return slots 0..cp_size-1; the one-shot sum of       */
 /* "Low Latency Communication Kernels with NVSHMEM", one-shot          */
 /* all-reduce). out[i] = ((s0[i] + s1[i]) + s2[i]) + ... in binary32,  */
 /* the accumulator starting from slot 0 itself (so -0.0 survives),     */
@@ -354,8 +354,8 @@ void oracle_slot_reduce(const void *const *slots, int P, int64_t n_elems,
 /* writers[w] is writer w's global gradient [T][row]; owners[o] is     */
 /* owner o's local gradient [T/P][row]. Owner o's local row j is       */
 /* global row g = l2g[o*T/P + j] and receives the ordered sum over     */
-/* w = 0..P-1 of writers[w][g] (the owner's own slot included:         */
-/* "all cp_size slots" in the diagram).                                */
+/* w = 0..P-1 of writers[w][g] (the owner's own slot included: the     */
+/* diagram sums every one of the cp_size slots).                       */
 /* Parity: pinned through the same closed forms as slot_reduce and the */
 /* map's pins.                                                         */
 /* ------------------------------------------------------------------ */
@@ -378,8 +378,8 @@ void oracle_grad_return(int P, int64_t T, int64_t row_elems, int in_dtype, int o
 
 /* ------------------------------------------------------------------ */
 /* Owner-gradient return that adds into the owner's existing gradient  */
-/* (the other reading of "accumulates four writer slots into the local */
-/* owner's dK/dV", [TE-3235] "Description"): the accumulator starts    */
+/* (the other reading of the accumulation step in [TE-3235]           */
+/* "Description"): the accumulator starts                              */
 /* from the owner's current value, then adds writers 0..P-1 in order:  */
 /*   out = round(((out + x_0) + x_1) + ... + x_{P-1}).                 */
 /* Parity: pinned (ones into ones, order canary with a start value,    */
