@@ -92,6 +92,7 @@ _sig("cpt_grad_scatter", ctypes.c_int, _vp, _i32, _vp, _vp, _vp, _i64, ctypes.c_
 _sig("cpt_epoch_create", ctypes.c_int, _i32, _vp, _vp, _vp, ctypes.POINTER(_vp))
 _sig("cpt_epoch_destroy", ctypes.c_int, _vp)
 _sig("cpt_epoch_advance", ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_uint32))
+_sig("cpt_epoch_set", ctypes.c_int, _vp, ctypes.c_uint32)
 _sig("cpt_epoch_publish", ctypes.c_int, _vp, _i32, _vp)
 _sig("cpt_epoch_wait", ctypes.c_int, _vp, _i32, _u64, ctypes.c_int, _vp)
 _sig("cpt_epoch_status", ctypes.c_int, _vp, _i32, _vp, ctypes.POINTER(_i32))
@@ -458,6 +459,10 @@ def cpt_epoch_advance(ep: Epoch) -> int:
     e = ctypes.c_uint32()
     _check(_lib.cpt_epoch_advance(ep.handle, ctypes.byref(e)))
     return e.value
+
+
+def cpt_epoch_set(ep: Epoch, epoch: int) -> None:
+    _check(_lib.cpt_epoch_set(ep.handle, epoch))
 
 
 def cpt_epoch_publish(ep: Epoch, writer: int, stream=None) -> None:

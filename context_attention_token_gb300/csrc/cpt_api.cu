@@ -886,6 +886,16 @@ cpt_status cpt_epoch_advance(cpt_epoch *ep, uint32_t *epoch_out)
     return CPT_OK;
 }
 
+cpt_status cpt_epoch_set(cpt_epoch *ep, uint32_t epoch)
+{
+    if (ep == nullptr) return fail(CPT_ERR_INVALID_ARG, "epoch is NULL");
+    if (epoch == 0) return fail(CPT_ERR_INVALID_ARG, "epoch 0 is reserved for \"never published\"");
+    std::lock_guard<std::mutex> lock(ep->mu);
+    ep->epoch = epoch;
+    for (int w = 0; w < CPT_MAX_CP_SIZE; ++w) ep->published[w] = 0;
+    return CPT_OK;
+}
+
 static cpt_status check_epoch(cpt_epoch *ep, int *dev)
 {
     if (ep == nullptr) return fail(CPT_ERR_INVALID_ARG, "epoch is NULL");

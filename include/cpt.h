@@ -439,6 +439,13 @@ CPT_API cpt_status cpt_epoch_destroy(cpt_epoch *ep);
  * only. `epoch_out` may be NULL. */
 CPT_API cpt_status cpt_epoch_advance(cpt_epoch *ep, uint32_t *epoch_out);
 
+/* Set the current epoch to `epoch` (non-zero), e.g. to resume a saved
+ * count, and forget which writers have published: every writer must
+ * publish `epoch` before an owner can wait on it. Host only; the device
+ * flags keep their values. Errors: CPT_ERR_INVALID_ARG for a NULL state or
+ * epoch 0. */
+CPT_API cpt_status cpt_epoch_set(cpt_epoch *ep, uint32_t epoch);
+
 /* Publish the current epoch from `writer` to every owner: P driver stream
  * writes flags[o*P + writer] = epoch, each ordered after all earlier work
  * on `stream` (with the driver's default memory barrier), then an event

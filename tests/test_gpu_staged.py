@@ -150,3 +150,106 @@ def test_epoch_api_errors(cpt, cuda_device):
     with pytest.raises(cpt.CptError) as ei:
         cpt.cpt_epoch_create(2, flags=host)
     assert ei.value.status == cpt.CPT_ERR_DEVICE
+
+
+def _staged_round(cpt, plan, writers, slots, out, ep, P, wstreams, ostreams, main,
+                  clear_flags_to=None, timeout_ns=2_000_000_000):
+    for w in range(P):
+        wstreams[w].wait_stream(main)
+        cpt.cpt_grad_scatter(plan, w, writers[w], [slots[o][w] for o in range(P)], slots[w][w],
+                             stream=wstreams[w])
+        cpt.cpt_epoch_publish(ep, w, stream=wstreams[w])
+    for o in range(P):
+        ostreams[o].wait_stream(main)
+        if clear_flags_to is not None:
+            for w in range(P):
+                ostreams[o].wait_stream(wstreams[w])
+            with torch.cuda.stream(ostreams[o]):
+                ep.flags.view(P, P)[o].fill_(clear_flags_to)
+        cpt.cpt_epoch_wait(ep, o, timeout_ns, 0, stream=ostreams[o])
+        cpt.cpt_slot_reduce([slots[o][w] for w in range(P)], out[o], ep.status_ptr(o), stream=ostreams[o])
+    for st in wstreams + ostreams:
+        main.wait_stream(st)
+    torch.cuda.synchronize()
+    return [cpt.cpt_epoch_status(ep, o) for o in range(P)]
+
+
+def test_epoch_count_wraps_around(cpt, cuda_device):
+    """Epochs run through 2^32 and wrap to 1 (0 is skipped); the flag test is
+    (int32)(flag - epoch) >= 0, so a stale pre-wrap flag 0xFFFFFFFF does not
+    satisfy epoch 1 although it is larger as an unsigned number."""
+    P = 2
+    cu, T, host, plan, writers = _setup(cpt, P, 0, [4 * 32])
+    slots = torch.empty((P, P, T // P, 4, 32), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((P, T // P, 4, 32), dtype=torch.bfloat16, device="cuda")
+    fused = torch.empty_like(out)
+    cpt.cpt_grad_return(plan, writers, None, fused, None)
+    ep = cpt.cpt_epoch_create(P)
+    main = torch.cuda.current_stream()
+    ws = [torch.cuda.Stream() for _ in range(P)]
+    os_ = [torch.cuda.Stream() for _ in range(P)]
+    cpt.cpt_epoch_set(ep, 0xFFFFFFFE)
+    assert _staged_round(cpt, plan, writers, slots, out, ep, P, ws, os_, main) == [0, 0]
+    assert cpt.cpt_epoch_advance(ep) == 0xFFFFFFFF
+    assert _staged_round(cpt, plan, writers, slots, out, ep, P, ws, os_, main) == [0, 0]
+    assert bool((ep.flags == -1).all().item())  # 0xFFFFFFFF in every flag
+    assert cpt.cpt_epoch_advance(ep) == 1  # wrapped, 0 skipped
+    assert _staged_round(cpt, plan, writers, slots, out, ep, P, ws, os_, main) == [0, 0]
+    assert torch.equal(out.view(torch.int16), fused.view(torch.int16))
+    # a stale pre-wrap value in the flags must not pass for epoch 2
+    assert cpt.cpt_epoch_advance(ep) == 2
+    out.fill_(9.0)
+    st = _staged_round(cpt, plan, writers, slots, out, ep, P, ws, os_, main,
+                       clear_flags_to=-1, timeout_ns=2_000_000)
+    assert st == [cpt.CPT_ERR_TIMEOUT] * P
+    assert bool((out == 9.0).all().item())
+    with pytest.raises(cpt.CptError):
+        cpt.cpt_epoch_set(ep, 0)
+
+
+def test_writers_publish_from_host_threads(cpt, cuda_device):
+    """Each writer rank is a host thread with its own stream; the C ABI is
+    called concurrently (the binding releases the GIL) and the epoch state
+    keeps its bookkeeping consistent."""
+    import threading
+
+    P = 4
+    cu, T, host, plan, writers = _setup(cpt, P, 0, [8 * 256], seed=9)
+    slots = torch.empty((P, P, T // P, 4, 32), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((P, T // P, 4, 32), dtype=torch.bfloat16, device="cuda")
+    fused = torch.empty_like(out)
+    cpt.cpt_grad_return(plan, writers, None, fused, None)
+    ep = cpt.cpt_epoch_create(P)
+    main = torch.cuda.current_stream()
+    wstreams = [torch.cuda.Stream() for _ in range(P)]
+    ostreams = [torch.cuda.Stream() for _ in range(P)]
+    errors = []
+
+    def writer(w):
+        try:
+            cpt.cpt_grad_scatter(plan, w, writers[w], [slots[o][w] for o in range(P)], slots[w][w],
+                                 stream=wstreams[w])
+            cpt.cpt_epoch_publish(ep, w, stream=wstreams[w])
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    for _ in range(5):
+        cpt.cpt_epoch_advance(ep)
+        for s in wstreams:
+            s.wait_stream(main)
+        threads = [threading.Thread(target=writer, args=(w,)) for w in range(P)]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+        assert not errors, errors
+        for o in range(P):
+            ostreams[o].wait_stream(main)
+            cpt.cpt_epoch_wait(ep, o, 2_000_000_000, 0, stream=ostreams[o])
+            cpt.cpt_slot_reduce([slots[o][w] for w in range(P)], out[o], ep.status_ptr(o),
+                                stream=ostreams[o])
+        for s in wstreams + ostreams:
+            main.wait_stream(s)
+        torch.cuda.synchronize()
+        assert [cpt.cpt_epoch_status(ep, o) for o in range(P)] == [0] * P
+        assert torch.equal(out.view(torch.int16), fused.view(torch.int16))
