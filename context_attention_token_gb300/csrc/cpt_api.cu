@@ -6,9 +6,8 @@
 // primitive", TransformerEngine PR 3235, author's reply on its size check):
 // device membership of every pointer (the page's "Greptile Summary" lists a
 // current-device guard on each tensor argument), alignment, sizes, overlaps
-// between outputs and
-// every other buffer of the call, and the self-slot alias of the staged
-// scatter. The driver's stream memory operations are resolved at run time
+// between outputs and every other buffer of the call, and the self-slot alias
+// of the staged scatter. The driver's stream memory operations are resolved at run time
 // through the runtime's driver entry-point query, so the library has no
 // link-time dependency on libcuda (same page, "Changes").
 #include "cpt.h"

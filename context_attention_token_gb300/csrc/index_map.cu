@@ -7,8 +7,9 @@
 // (TransformerEngine PR 3235), author's reply: owner o receives chunks o and
 // 2N-1-o.
 //
-// Both kernels are integer-only and move a few bytes per token; they are
-// launch-bound at the sizes used here, so they favour simplicity.
+// The kernels here (the map, the metadata, the padded layout's extra maps
+// and the real-token counts) are integer-only and move a few bytes per token;
+// they are launch-bound at the sizes used here, so they favour simplicity.
 #include "cpt_internal.h"
 
 namespace cpt {

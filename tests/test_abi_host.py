@@ -126,3 +126,30 @@ def test_padded_layout_validation(cpt):
     assert cpt.cpt_plan_workspace_bytes(PAD, 4, 3, 12) >= cpt.cpt_plan_workspace_bytes(0, 4, 3, 12)
     big = 2**31 - 8
     assert cpt.cpt_validate_layout(PAD, 8, [0, 1, big], big) == cpt.CPT_ERR_INVALID_ARG
+
+
+def test_binding_constants_match_header(cpt):
+    """Every enumerator and #define of include/cpt.h has the same value in the binding."""
+    import re
+
+    with open(HEADER) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    consts = {}
+    for body in re.findall(r"typedef enum \w+ \{(.*?)\}", text, flags=re.S):
+        nxt = 0
+        for item in body.split(","):
+            item = item.strip()
+            if not item:
+                continue
+            if "=" in item:
+                name, val = (x.strip() for x in item.split("="))
+                nxt = int(val, 0)
+            else:
+                name = item
+            consts[name] = nxt
+            nxt += 1
+    for name, val in re.findall(r"#define (CPT_[A-Z0-9_]+) (\d+)", text):
+        consts[name] = int(val)
+    assert len(consts) >= 20
+    for name, val in consts.items():
+        assert getattr(cpt, name) == val, name
