@@ -601,6 +601,39 @@ def run_next_rows(args):
         del dkw, dvw, dko, dvo
         torch.cuda.empty_cache()
 
+    # the other grad_return shapes of the survey's configurations: the
+    # single-document case (S=32768, 8x128; its 0.67 GB are close to L2 size,
+    # so each launch is preceded by a 512 MB write that flushes L2) and the
+    # lognormal packed batch (T=131072, 16x128) under both layouts
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for name, Tg, Hg, lens_g in (("grad_return_single_doc_S32768_8x128", 32768, 8, [32768]),
+                                 ("grad_return_lognormal_T131072_16x128_dsc", 131072, 16,
+                                  synth.lognormal_doc_lengths(131072, synth.rng_for(2, 0), multiple=8)),
+                                 ("grad_return_lognormal_T131072_16x128_packed", 131072, 16,
+                                  synth.lognormal_doc_lengths(131072, synth.rng_for(2, 0)))):
+        layout_g = 1 if name.endswith("packed") else 0
+        plg = cpt.cpt_plan_create(layout_g, P, synth.cu_from_lengths(lens_g), Tg)
+        wk = synth.device_normal_bf16((P, Tg, Hg, D), 6400, 1.0, "cuda")
+        wv = synth.device_normal_bf16((P, Tg, Hg, D), 6401, 1.0, "cuda")
+        ok = torch.empty((P, Tg // P, Hg, D), dtype=torch.bfloat16, device="cuda")
+        ov = torch.empty_like(ok)
+        evs = []
+        for it in range(23):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            cpt.cpt_grad_return(plg, wk, wv, ok, ov)
+            b.record(stream)
+            if it >= 3:
+                evs.append((a, b))
+        torch.cuda.synchronize()
+        ms = statistics.median(x.elapsed_time(y) for x, y in evs)
+        emit(name, ms, Tg * (2 * (P + 1) * Hg * D * 2 + 2 * 4), P=P, T=Tg, docs=len(lens_g),
+             l2="flushed before each launch")
+        del wk, wv, ok, ov
+        torch.cuda.empty_cache()
+    del flush
+
     # f3 / matched inputs: one lognormal batch (lengths multiples of 8 so all
     # three policies accept it), Q/K/V [T,16,128]
     T, Hq = 131072, 16
