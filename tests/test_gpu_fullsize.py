@@ -157,3 +157,57 @@ def test_largest_batch_the_maps_allow(cpt, cuda_device):
         assert torch.equal(blk[:, 0], l2g[a:b]) and bool((blk == blk[:, :1]).all().item())
     del src, dst, flat, l2g
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_grad_return_lognormal_batch_sampled(cpt, cuda_device, layout):
+    """Packed THD configuration: T=131072 from lognormal documents, writers
+    [4, T, 16, 128] bf16 N(0,1), both layouts, sampled owner rows against
+    the oracle (document boundaries included in the sample)."""
+    Pl, Tl, Hl = 4, 131072, 16
+    lens = synth.lognormal_doc_lengths(Tl, synth.rng_for(2, 0), multiple=8 if layout == 0 else 1)
+    cu = synth.cu_from_lengths(lens)
+    plan = cpt.cpt_plan_create(layout, Pl, cu, Tl)
+    l2g, g2l = oracle.index_map(layout, Pl, cu, Tl)
+    wk = synth.device_normal_bf16((Pl, Tl, Hl, D), 4101 + layout, 1.0, "cuda")
+    wv = synth.device_normal_bf16((Pl, Tl, Hl, D), 4111 + layout, 1.0, "cuda")
+    ok = torch.empty((Pl, Tl // Pl, Hl, D), dtype=torch.bfloat16, device="cuda")
+    ov = torch.empty_like(ok)
+    cpt.cpt_grad_return(plan, wk, wv, ok, ov)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(46)
+    edges = np.clip(np.concatenate([cu[:-1], cu[1:] - 1]), 0, Tl - 1)
+    q = np.unique(np.concatenate([g2l[edges], rng.integers(0, Tl, size=4000)])).astype(np.int64)
+    g = torch.from_numpy(l2g[q].astype(np.int64)).cuda()
+    qd = torch.from_numpy(q).cuda()
+    for w_all, out in ((wk, ok), (wv, ov)):
+        ins = [to_host(w_all[w].index_select(0, g)) for w in range(Pl)]
+        want = oracle.slot_reduce(ins, oracle.BF16)
+        got = to_host(out.view(Tl, Hl, D).index_select(0, qd))
+        assert np.array_equal(got, want)
+    del wk, wv, ok, ov
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_slot_reduce_one_gigabyte_slots_sampled(cpt, cuda_device, dtype):
+    """Slot-reduce configuration at its largest message: 8 slots of 1 GB
+    (plus a ragged tail of 3 elements), sampled elements against the oracle."""
+    esz = torch.tensor([], dtype=dtype).element_size()
+    n = (1 << 30) // esz + 3
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(4200 + esz)
+    slots = [(torch.rand(n, device="cuda", generator=gen) * 2 - 1).to(dtype) for _ in range(8)]
+    dst = torch.empty(n, dtype=dtype, device="cuda")
+    cpt.cpt_slot_reduce(slots, dst)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(47)
+    idx = np.unique(np.concatenate([rng.integers(0, n, size=100000), np.arange(n - 11, n)]))
+    ii = torch.from_numpy(idx.astype(np.int64)).cuda()
+    ins = [to_host(s.index_select(0, ii)) for s in slots]
+    want = oracle.slot_reduce(ins, oracle.BF16 if dtype == torch.bfloat16 else oracle.F32)
+    got = to_host(dst.index_select(0, ii))
+    from gpu_helpers import bits
+    assert np.array_equal(bits(got), bits(want))
+    del slots, dst
+    torch.cuda.empty_cache()
