@@ -59,7 +59,7 @@ __device__ __forceinline__ void widen_f32(const uint4 &v, float (&f)[4])
 }
 
 template <int P, int IN, int OUT, int U>
-__global__ void __launch_bounds__(kThreads) slot_reduce_kernel(const SlotReduceParams p)
+__global__ void __launch_bounds__(kThreads, 4) slot_reduce_kernel(const SlotReduceParams p)
 {
     if (p.status != nullptr && *reinterpret_cast<const volatile int32_t *>(p.status) != 0) return;
     constexpr int E = IN == kBf16 ? 8 : 4;
