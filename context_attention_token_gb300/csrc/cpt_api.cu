@@ -392,7 +392,12 @@ cpt_status cpt_plan_create(cpt_layout layout, int32_t P, const int32_t *cu, int3
     p->g2l = reinterpret_cast<int32_t *>(base + w.g2l);
     if (pad) {
         // every document padded up to a multiple of 2P
-        p->h_cup.resize((size_t)n + 1);
+        try {
+            p->h_cup.resize((size_t)n + 1);
+        } catch (const std::bad_alloc &) {
+            delete p;
+            return fail(CPT_ERR_INVALID_ARG, "out of host memory");
+        }
         p->h_cup[0] = 0;
         for (int32_t i = 0; i < n; ++i) {
             const int32_t L = cu[i + 1] - cu[i];
@@ -1044,7 +1049,11 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
     int64_t Tmap = T;
     int map_layout = (int)layout;
     if (is_padded(layout)) {
-        cup.resize((size_t)n + 1);
+        try {
+            cup.resize((size_t)n + 1);
+        } catch (const std::bad_alloc &) {
+            return fail(CPT_ERR_INVALID_ARG, "out of host memory");
+        }
         cup[0] = 0;
         for (int32_t i = 0; i < n; ++i) {
             const int32_t L = cu[i + 1] - cu[i];

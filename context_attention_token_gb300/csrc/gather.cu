@@ -63,20 +63,20 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p)
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream)
 {
     if (p.rows == 0) return cudaSuccess;
-    static thread_local int cached_dev = -1, cached_blocks = 0;
+    static int blocks_per_sm[64] = {0};  // per device
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev != cached_dev) {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (blocks_per_sm[dev] == 0) {
         int per_sm = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel,
-                                                                      kThreads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel, kThreads, 0);
         if (e != cudaSuccess) return e;
-        cached_blocks = per_sm * sm_count(dev);
-        cached_dev = dev;
+        blocks_per_sm[dev] = per_sm > 0 ? per_sm : 1;
     }
-    const int64_t warps_needed = p.rows;
-    int64_t blocks = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
-    if (blocks > cached_blocks) blocks = cached_blocks;
+    const int64_t cap = (int64_t)blocks_per_sm[dev] * sm_count(dev);
+    int64_t blocks = (p.rows + (kThreads / 32) - 1) / (kThreads / 32);  // one warp per row
+    if (blocks > cap) blocks = cap;
     gather_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }

@@ -156,7 +156,8 @@ cudaError_t launch_typed(const GradReturnParams &p, cudaStream_t stream)
     auto kernel = grad_return_kernel<P, IN, OUT, U, ACC>;
     static int blocks_per_sm[64] = {0};  // per device, one table per instantiation
     int dev = 0;
-    cudaGetDevice(&dev);
+    const cudaError_t dev_err = cudaGetDevice(&dev);
+    if (dev_err != cudaSuccess) return dev_err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (blocks_per_sm[dev] == 0) {
         int n = 0;

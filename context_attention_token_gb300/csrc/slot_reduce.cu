@@ -127,7 +127,8 @@ cudaError_t launch_typed(const SlotReduceParams &p, cudaStream_t stream)
     auto kernel = slot_reduce_kernel<P, IN, OUT, U>;
     static int blocks_per_sm[64] = {0};
     int dev = 0;
-    cudaGetDevice(&dev);
+    const cudaError_t dev_err = cudaGetDevice(&dev);
+    if (dev_err != cudaSuccess) return dev_err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (blocks_per_sm[dev] == 0) {
         int n = 0;
