@@ -223,10 +223,93 @@ def oracle_sample_step_factory(tokens: int):
     return step
 
 
+def _oracle_replica(tokens, heads, mode, count, budget_s, barrier, results):
+    """One process of the all-cores oracle timing (spawned; module globals
+    are the defaults there, so the head count comes in as an argument).
+
+    mode "budget": after the common start, run passes until budget_s has
+    passed and report (passes, seconds). mode "steps": run `count` passes,
+    each started by a barrier that the parent also joins, so the parent
+    times whole steps across all replicas."""
+    global H
+    H = heads
+    step = oracle_sample_step_factory(tokens)
+    step()  # page in the inputs
+    if mode == "budget":
+        barrier.wait()
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            step()
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget_s:
+                break
+        results.put((reps, dt))
+    else:
+        for _ in range(count):
+            barrier.wait(timeout=600)
+            step()
+        barrier.wait(timeout=600)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def replica_count(tokens: int, want: int) -> int:
+    """Cores to use, capped so that the replicas' inputs and outputs (about
+    16 rows of every token each) stay under a quarter of host memory."""
+    per = 16 * tokens * row_bytes()
+    try:
+        mem = os.sysconf("SC_PHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError):
+        mem = 0
+    cap = max(1, int(0.25 * mem // per)) if mem else 1
+    return max(1, min(want, cap))
+
+
+def _spawn_replicas(n, tokens, mode, count, budget_s, parties):
+    import multiprocessing as mp
+
+    import oracle
+
+    oracle.build()  # once here, not in every replica
+    ctx = mp.get_context("spawn")  # never fork a process that holds a CUDA context
+    barrier = ctx.Barrier(parties)
+    results = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_replica, args=(tokens, H, mode, count, budget_s, barrier, results),
+                         daemon=True) for _ in range(n)]
+    for pr in procs:
+        pr.start()
+    return procs, barrier, results
+
+
+def oracle_all_cores(tokens: int, budget_s: float, cores: int):
+    """The unmodified oracle on `cores` host cores at once: independent
+    single-threaded replicas of the same sample, each in its own process.
+    value = bytes of all passes of all replicas / the longest replica time."""
+    procs, _barrier, results = _spawn_replicas(cores, tokens, "budget", 0, budget_s, cores)
+    # (_barrier stays bound until the replicas are joined, for the same reason)
+    got = [results.get(timeout=600) for _ in procs]
+    for pr in procs:
+        pr.join(timeout=60)
+    reps = sum(r for r, _ in got)
+    dt = max(t for _, t in got)
+    return {"value": step_bytes(tokens) * reps / dt / 1e9, "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": (f"{cores} single-threaded oracle replicas in parallel, {reps} passes in all "
+                       f"of the whole path over {tokens} of {S} tokens (same P=4, {H}x{D} bf16 "
+                       f"single document), {dt:.1f} s")}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    cores = args.reference_cores or host_cores()
     tokens = args.sample_tokens
     if not args.fixed_sample:
         # size the sample so the whole run takes about args.reference_budget
@@ -242,30 +325,44 @@ def run_reference(args):
         tokens = 256
         while tokens * 2 <= min(fit, args.sample_tokens):
             tokens *= 2
-    step = oracle_sample_step_factory(tokens)
+    cores = replica_count(tokens, cores)
+    # every step: each of `cores` replicas makes one oracle pass over its
+    # sample; the parent joins the barrier that starts each step
+    # keep the queue bound: collecting it unlinks semaphores the children still need
+    procs, barrier, _results = _spawn_replicas(cores, tokens, "steps", args.warmup + args.steps,
+                                               0.0, cores + 1)
     for _ in range(args.warmup):
-        step()
+        barrier.wait(timeout=600)
+    barrier.wait(timeout=600)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
+    for _ in range(args.steps - 1):
+        barrier.wait(timeout=600)
+    barrier.wait(timeout=600)
     dt = time.perf_counter() - t0
-    value = step_bytes(tokens) * args.steps / dt / 1e9
-    sample = (f"{tokens} of {S} tokens per step (same P=4, 20x128 bf16, single document); "
-              f"whole path: maps, metadata, 3-tensor partition, dK+dV grad_return")
+    for pr in procs:
+        pr.join(timeout=60)
+    value = step_bytes(tokens) * cores * args.steps / dt / 1e9
+    sample = (f"{cores} x {tokens} of {S} tokens per step: {cores} single-threaded oracle replicas "
+              f"in parallel, each over the same P=4, {H}x{D} bf16 single document; whole path: "
+              f"maps, metadata, 3-tensor partition, dK+dV grad_return")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": workload(), "P": P, "S": S, "H": H, "D": D, "sample_tokens": tokens},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "config": {"workload": workload(), "P": P, "S": S, "H": H, "D": D, "sample_tokens": tokens,
+                   "replicas": cores},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def cpu_baseline(tokens: int, budget_s: float):
+def cpu_baseline(tokens: int, budget_s: float, cores: int = 0):
+    """The oracle on one core, then (cores > 1) on `cores` cores at once.
+    The all-cores figure is the line's baseline; the one-core one rides along."""
     step = oracle_sample_step_factory(tokens)
     step()  # warm caches and page in the inputs
     reps, t0 = 0, time.perf_counter()
@@ -275,10 +372,16 @@ def cpu_baseline(tokens: int, budget_s: float):
         dt = time.perf_counter() - t0
         if dt >= budget_s:
             break
-    return {"value": step_bytes(tokens) * reps / dt / 1e9, "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
-            "sample": (f"{reps} oracle passes of the whole path over {tokens} of {S} tokens "
-                       f"(same P=4, 20x128 bf16 single document), {dt:.1f} s single-threaded")}
+    one = {"value": step_bytes(tokens) * reps / dt / 1e9, "unit": "GB/s", "cores": 1,
+           "kind": "oracle",
+           "sample": (f"{reps} oracle passes of the whole path over {tokens} of {S} tokens "
+                      f"(same P=4, {H}x{D} bf16 single document), {dt:.1f} s single-threaded")}
+    cores = replica_count(tokens, cores)
+    if cores <= 1:
+        return one
+    out = oracle_all_cores(tokens, budget_s, cores)
+    out["single_core"] = one
+    return out
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -520,7 +623,8 @@ def run_gpu(args):
         "e2e": e2e,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.sample_tokens, args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(args.sample_tokens, args.cpu_budget,
+                                            args.cpu_cores or host_cores())
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -762,7 +866,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sample-tokens", type=int, default=16384,
                     help="tokens of the workload the CPU oracle processes per pass")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work, for each of the one-core and all-cores legs")
+    ap.add_argument("--cpu-cores", type=int, default=0,
+                    help="host cores for the all-cores oracle leg (0 = every core this process may use)")
+    ap.add_argument("--reference-cores", type=int, default=0,
+                    help="--impl reference: parallel oracle replicas (0 = every core)")
     ap.add_argument("--reference-budget", type=float, default=120.0,
                     help="target seconds for a whole --impl reference run")
     ap.add_argument("--fixed-sample", action="store_true",
@@ -783,6 +892,8 @@ def main():
     if S % (2 * P) or S <= 0 or H <= 0:
         ap.error("--tokens must be a positive multiple of 8, --heads positive")
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep == "slot_reduce":
