@@ -386,6 +386,27 @@ def cpu_baseline(tokens: int, budget_s: float, cores: int = 0):
 
 # ---------------------------------------------------------------- GPU arm
 
+def copy_ceiling_gbs(dev, stream) -> float:
+    """A plain device-to-device copy timed in the same run, as a practical
+    ceiling beside the recorded peak: 1 Gi bf16 elements (2 GiB read + 2 GiB
+    written), CUDA events on the launching stream, best of 10 after 3."""
+    import torch
+
+    a = torch.ones(1 << 30, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    best = float("inf")
+    for i in range(13):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        b.copy_(a)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            best = min(best, e0.elapsed_time(e1))
+    del a, b
+    return 2 * (1 << 30) * 2 / (best / 1e3) / 1e9
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -505,6 +526,7 @@ def run_gpu(args):
     part_ms = [a.elapsed_time(b) for a, b in ev_part]
 
     max_ms = max_over_ranks(elapsed_ms, dev)
+    copy_gbs = copy_ceiling_gbs(dev, stream)
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -516,7 +538,6 @@ def run_gpu(args):
         h2d = sum(x.numel() * x.element_size() for x in host_in)
         d2h = sum(x.numel() * x.element_size() for x in host_out)
 
-        side = torch.cuda.Stream()
         h_qkv, h_dkw, h_dvw = host_in[:3], host_in[3], host_in[4]
         h_part, h_dko, h_dvo = host_out[:3], host_out[3], host_out[4]
 
@@ -539,33 +560,51 @@ def run_gpu(args):
         del probe, g2l_dev, l2g_dev
         flat = lambda t: t.view(S, H, D)  # noqa: E731  rank-major local tensor as [S, H, D]
 
+        # Pieces: every global chunk of m tokens cut into `pieces` runs of
+        # local rows, so the last piece's copy out (the pipeline's tail) is short.
+        pieces = []
+        for g0, q0 in chunks:
+            cut = [m * i // args.e2e_pieces for i in range(args.e2e_pieces + 1)]
+            pieces += [(g0 + a, q0 + a, b - a) for a, b in zip(cut, cut[1:]) if b > a]
+        h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+
         def e2e_step():
-            # Two independent chains on two streams, each pipelined over the 2P
-            # global chunks: chunk k's host-to-device copies overlap the
-            # kernels and device-to-host copies of chunk k-1.
-            #   main: Q/K/V rows in -> partition of their local rows -> out
-            #   side: dK/dV rows of every writer in -> grad_return of their
-            #         local rows -> owner rows out
+            # Three streams, one per resource: host-to-device copies of every
+            # piece back to back on h2d_stream, the kernels of a piece on the
+            # main stream once its rows are in, its rows out on d2h_stream once
+            # its kernels are done. A step starts after the previous one ended
+            # on every stream, so no buffer is overwritten while still in use.
+            h2d_stream.wait_stream(stream)
+            d2h_stream.wait_stream(stream)
             plan = cpt.cpt_plan_create(cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP, P, cu, S, workspace=ws)
-            plan_ready = torch.cuda.Event()
-            plan_ready.record(stream)
-            side.wait_event(plan_ready)
-            for g0, q0 in chunks:
-                for d, h in zip(qkv, h_qkv):
-                    d[g0:g0 + m].copy_(h[g0:g0 + m], non_blocking=True)
-                cpt.cpt_partition_rows(plan, qkv, part, q0, m)
-                for h, d in zip(h_part, part):
-                    flat(h)[q0:q0 + m].copy_(flat(d)[q0:q0 + m], non_blocking=True)
-                with torch.cuda.stream(side):
+            for g0, q0, c in pieces:
+                with torch.cuda.stream(h2d_stream):
+                    for d, h in zip(qkv, h_qkv):
+                        d[g0:g0 + c].copy_(h[g0:g0 + c], non_blocking=True)
+                    qkv_in = torch.cuda.Event()
+                    qkv_in.record(h2d_stream)
                     for w in range(P):
-                        dkw[w, g0:g0 + m].copy_(h_dkw[w, g0:g0 + m], non_blocking=True)
-                        dvw[w, g0:g0 + m].copy_(h_dvw[w, g0:g0 + m], non_blocking=True)
-                cpt.cpt_grad_return_rows(plan, dkw, dvw, dko, dvo, q0, m, stream=side)
-                with torch.cuda.stream(side):
-                    flat(h_dko)[q0:q0 + m].copy_(flat(dko)[q0:q0 + m], non_blocking=True)
-                    flat(h_dvo)[q0:q0 + m].copy_(flat(dvo)[q0:q0 + m], non_blocking=True)
-            stream.wait_stream(side)
-            side.wait_stream(stream)
+                        dkw[w, g0:g0 + c].copy_(h_dkw[w, g0:g0 + c], non_blocking=True)
+                        dvw[w, g0:g0 + c].copy_(h_dvw[w, g0:g0 + c], non_blocking=True)
+                    grads_in = torch.cuda.Event()
+                    grads_in.record(h2d_stream)
+                stream.wait_event(qkv_in)
+                cpt.cpt_partition_rows(plan, qkv, part, q0, c)
+                part_done = torch.cuda.Event()
+                part_done.record(stream)
+                stream.wait_event(grads_in)
+                cpt.cpt_grad_return_rows(plan, dkw, dvw, dko, dvo, q0, c)
+                grads_done = torch.cuda.Event()
+                grads_done.record(stream)
+                with torch.cuda.stream(d2h_stream):
+                    d2h_stream.wait_event(part_done)
+                    for h, d in zip(h_part, part):
+                        flat(h)[q0:q0 + c].copy_(flat(d)[q0:q0 + c], non_blocking=True)
+                    d2h_stream.wait_event(grads_done)
+                    flat(h_dko)[q0:q0 + c].copy_(flat(dko)[q0:q0 + c], non_blocking=True)
+                    flat(h_dvo)[q0:q0 + c].copy_(flat(dvo)[q0:q0 + c], non_blocking=True)
+            stream.wait_stream(h2d_stream)
+            stream.wait_stream(d2h_stream)
             cpt.cpt_plan_destroy(plan)
 
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -582,7 +621,8 @@ def run_gpu(args):
         e2e_ms = max_over_ranks(a.elapsed_time(b), dev) / e2e_steps
         e2e = {"value": whole_job_gbs(step_bytes(S), 1, world, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "steps": e2e_steps}
+               "steps": e2e_steps,
+               "pipeline": f"copies in, kernels, copies out on 3 streams over {len(pieces)} pieces"}
         del host_in, host_out
 
     if rank != 0:
@@ -618,6 +658,10 @@ def run_gpu(args):
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6800 GB/s", "unit": "GB/s", "frac": gr_gbs / peak,
                      "traffic": profiled_traffic("grad_return", S) if PATH == "fused" else None},
+        "copy_ceiling": {"gbs": copy_gbs, "grad_return_frac": gr_gbs / copy_gbs,
+                         "partition_frac": part_gbs / copy_gbs,
+                         "how": "torch copy_ of 1 Gi bf16 elements in this run, read+write bytes, "
+                                "best of 10 after 3, CUDA events"},
         "clocks": sampler.summary(t_wall0, t_wall1),
         "gpu_launches": kernels_per_step * args.steps,
         "e2e": e2e,
@@ -770,6 +814,59 @@ def run_next_rows(args):
 
 # ---------------------------------------------------------------- slot-reduce sweep
 
+def run_host_link_sweep(args):
+    """The host link under the e2e step: 2 GiB between pinned host memory and
+    HBM by cudaMemcpyAsync, one direction at a time and both at once on two
+    streams, best of 5 after a warm-up. One JSON line."""
+    import torch
+
+    torch.cuda.set_device(0)
+    nbytes = 2 << 30
+    h_src = torch.ones(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_dst = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_src = torch.ones(nbytes, dtype=torch.uint8, device="cuda")
+    d_dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+
+    def best_ms(fn):
+        ms = []
+        for i in range(6):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(main)
+            s_in.wait_stream(main)
+            s_out.wait_stream(main)
+            fn()
+            main.wait_stream(s_in)
+            main.wait_stream(s_out)
+            e1.record(main)
+            torch.cuda.synchronize()
+            if i:
+                ms.append(e0.elapsed_time(e1))
+        return min(ms)
+
+    def h2d():
+        with torch.cuda.stream(s_in):
+            d_dst.copy_(h_src, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s_out):
+            h_dst.copy_(d_src, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    gbs = lambda n, ms: n / (ms / 1e3) / 1e9  # noqa: E731
+    line = {"sweep": "host_link", "bytes_per_direction": nbytes, "unit": "GB/s",
+            "h2d": gbs(nbytes, best_ms(h2d)), "d2h": gbs(nbytes, best_ms(d2h)),
+            "both_total": gbs(2 * nbytes, best_ms(both)),
+            "how": "cudaMemcpyAsync between pinned host memory and HBM, CUDA events, best of 5"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_slot_reduce_sweep(args):
     """P=8 slot buffers of N bytes each, N = 1 KB x 4^k up to 1 GB, float32 and
     bf16: one ordered sum per launch. One JSON line per (dtype, N), with the
@@ -863,6 +960,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-pieces", type=int, default=2,
+                    help="pieces each of the 2P global chunks is cut into for the e2e pipeline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sample-tokens", type=int, default=16384,
                     help="tokens of the workload the CPU oracle processes per pass")
@@ -882,8 +981,9 @@ def main():
     ap.add_argument("--next-rows", action="store_true",
                     help="instead of the step: restore, accumulate, P sweep, no-alloc and "
                          "partition-policy lines")
-    ap.add_argument("--sweep", choices=["slot_reduce"], default=None,
-                    help="instead of the step: the slot-reduce message-size sweep")
+    ap.add_argument("--sweep", choices=["slot_reduce", "host_link"], default=None,
+                    help="instead of the step: the slot-reduce message-size sweep, or the "
+                         "host link's copy rates")
     ap.add_argument("--tokens", type=int, default=S, help="S (multiple of 2P)")
     ap.add_argument("--heads", type=int, default=H)
     args = ap.parse_args()
@@ -898,6 +998,8 @@ def main():
         return run_reference(args)
     if args.sweep == "slot_reduce":
         return run_slot_reduce_sweep(args)
+    if args.sweep == "host_link":
+        return run_host_link_sweep(args)
     if args.next_rows:
         return run_next_rows(args)
     return run_gpu(args)
