@@ -720,6 +720,73 @@ def run_next_rows(args):
                 "peak": peak, "peak_source": peak_src, **extra}
         print(json.dumps(line), flush=True)
 
+    # integer metadata: launch-bound, reported as latency. Per configuration:
+    # the plan (cu_seqlens copy + map and metadata kernels) as host wall time
+    # of the call and as device time between events; the stand-alone map and
+    # metadata calls as device time; both as CUDA-graph replays per pair.
+    lat_cases = (
+        ("tiny_T64_P2_dsc", 0, 2, [16, 24, 24]),
+        ("tiny_T64_P2_packed", 1, 2, [16, 24, 24]),
+        ("single_doc_S32768_P4", 0, P, [32768]),
+        ("lognormal_T131072_P4_dsc", 0, P,
+         synth.lognormal_doc_lengths(131072, synth.rng_for(2, 0), multiple=8)),
+        ("lognormal_T131072_P4_packed", 1, P, synth.lognormal_doc_lengths(131072, synth.rng_for(2, 0))),
+        ("lognormal_T131072_P4_padded", 3, P, synth.lognormal_doc_lengths(131072, synth.rng_for(2, 0))),
+        ("pages_S262144_P4", 0, P, [S]),
+    )
+    for name, layout, Pl, lens_l in lat_cases:
+        cu_l = synth.cu_from_lengths(lens_l)
+        T_l, n_l = int(cu_l[-1]), len(lens_l)
+        ws_l = torch.empty(cpt.cpt_plan_workspace_bytes(layout, Pl, n_l, T_l), dtype=torch.uint8,
+                           device="cuda")
+        host_us, dev_ms = [], []
+        for it in range(23):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            t0 = time.perf_counter()
+            pl = cpt.cpt_plan_create(layout, Pl, cu_l, T_l, workspace=ws_l)
+            t1 = time.perf_counter()
+            b.record(stream)
+            torch.cuda.synchronize()
+            cpt.cpt_plan_destroy(pl)
+            if it >= 3:
+                host_us.append((t1 - t0) * 1e6)
+                dev_ms.append(a.elapsed_time(b))
+        pl = cpt.cpt_plan_create(layout, Pl, cu_l, T_l, workspace=ws_l)
+        Tp_l = pl.padded_tokens
+        l2g_l = torch.empty(Tp_l, dtype=torch.int32, device="cuda")
+        g2l_l = torch.empty(Tp_l, dtype=torch.int32, device="cuda")
+        meta = (torch.empty(Pl, dtype=torch.int32, device="cuda"),
+                torch.empty(Pl, dtype=torch.int32, device="cuda"),
+                torch.empty((Pl, n_l + 1), dtype=torch.int32, device="cuda"),
+                torch.empty(Pl + 1, dtype=torch.int32, device="cuda"))
+        map_ms = _median_launch_ms(lambda: cpt.cpt_index_map(pl, l2g_l, g2l_l), stream)
+        meta_ms = _median_launch_ms(lambda: cpt.cpt_thd_metadata(pl, *meta), stream)
+        side = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        reps = 20
+        with torch.cuda.stream(side):
+            cpt.cpt_index_map(pl, l2g_l, g2l_l, stream=side)
+            cpt.cpt_thd_metadata(pl, *meta, stream=side)
+            side.synchronize()
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(reps):
+                    cpt.cpt_index_map(pl, l2g_l, g2l_l, stream=side)
+                    cpt.cpt_thd_metadata(pl, *meta, stream=side)
+        graph.replay()
+        torch.cuda.synchronize()
+        graph_ms = _median_launch_ms(graph.replay, stream, reps=10)
+        print(json.dumps({"metadata_latency": name, "layout": layout, "P": Pl, "T": T_l,
+                          "T_padded": Tp_l, "docs": n_l,
+                          "plan_create_host_us": statistics.median(host_us),
+                          "plan_create_device_us": statistics.median(dev_ms) * 1e3,
+                          "index_map_device_us": map_ms * 1e3,
+                          "thd_metadata_device_us": meta_ms * 1e3,
+                          "map_plus_metadata_graph_us": graph_ms * 1e3 / reps}), flush=True)
+        cpt.cpt_plan_destroy(pl)
+        del graph, ws_l, l2g_l, g2l_l, meta
+
     # f1: restore K and V from rank-local back to global order
     plan = cpt.cpt_plan_create(0, P, [0, S], S)
     kv = [synth.device_normal_bf16((P, S // P, H, D), 6000 + t, 1.0, "cuda") for t in range(2)]
