@@ -96,6 +96,7 @@ _sig("cpt_epoch_set", ctypes.c_int, _vp, ctypes.c_uint32)
 _sig("cpt_epoch_publish", ctypes.c_int, _vp, _i32, _vp)
 _sig("cpt_epoch_wait", ctypes.c_int, _vp, _i32, _u64, ctypes.c_int, _vp)
 _sig("cpt_epoch_status", ctypes.c_int, _vp, _i32, _vp, ctypes.POINTER(_i32))
+_sig("cpt_kernel_wait_timeouts", ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), _i32)
 _sig("cpt_slot_reduce", ctypes.c_int, _vp, _i32, _i64, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp)
 
 
@@ -477,6 +478,15 @@ def cpt_epoch_wait(ep: Epoch, owner: int, timeout_ns: int = 1_000_000_000,
 def cpt_epoch_status(ep: Epoch, owner: int, stream=None) -> int:
     v = _i32()
     _check(_lib.cpt_epoch_status(ep.handle, owner, _stream(stream), ctypes.byref(v)))
+    return v.value
+
+
+def cpt_kernel_wait_timeouts(reset: bool = False) -> int:
+    """Bulk-copy waits in the library's kernels that ran out of their budget
+    on the current device (blocking; non-zero means an earlier output is not
+    valid)."""
+    v = ctypes.c_uint32()
+    _check(_lib.cpt_kernel_wait_timeouts(ctypes.byref(v), 1 if reset else 0))
     return v.value
 
 

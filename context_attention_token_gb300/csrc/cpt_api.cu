@@ -997,6 +997,19 @@ cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *stream, in
     return CPT_OK;
 }
 
+cpt_status cpt_kernel_wait_timeouts(uint32_t *count, int32_t reset)
+{
+    Trace trace("cpt_kernel_wait_timeouts");
+    if (count == nullptr) return fail(CPT_ERR_INVALID_ARG, "NULL argument");
+    int dev = 0;
+    if (!current_device(&dev)) return fail(CPT_ERR_DEVICE, "no current CUDA device");
+    unsigned int v = 0;
+    const cudaError_t e = read_wait_timeouts(&v, reset != 0);
+    if (e != cudaSuccess) return cuda_fail(e, "wait-timeout counter read");
+    *count = v;
+    return CPT_OK;
+}
+
 }  // extern "C"
 
 // ----------------------------------------------------------------- no allocation

@@ -68,6 +68,11 @@ struct GradReturnParams {
     int32_t in_row_bytes;
     int32_t out_row_bytes;
 };
+// Reads (and, if reset, zeroes) the count of bulk-copy waits in the gradient
+// return kernel that ran out of their budget, on the current device.
+// Synchronous.
+cudaError_t read_wait_timeouts(unsigned int *count, bool reset);
+
 cudaError_t launch_grad_return(const GradReturnParams &p, int cp_size, int in_dtype,
                                int out_dtype, cudaStream_t stream, bool accumulate = false);
 

@@ -7,10 +7,20 @@
 // binary32 in writer order 0..P-1 starting from writer 0's value, rounded
 // once, and stored. dK and dV go through the same launch.
 //
-// HBM-bound: per output row it reads P input rows and writes one. A warp owns
-// one output row at a time; each lane keeps kUnroll x P 16-byte loads in
-// flight before summing, and the grid is a whole number of CTAs per SM, each
-// warp striding over rows in output order.
+// HBM-bound: per output row it reads P input rows and writes one. Two kernels
+// share the arithmetic (binary32 adds in writer order):
+//  - grad_return_bulk_kernel, for equal input and output types, overwrite,
+//    and the cp_size / row sizes where it measured faster (prefer_bulk): every
+//    warp runs its own row pipeline.
+//    Lane 0 brings the P writer rows into shared memory with P bulk copies
+//    (cp.async.bulk) counted on one mbarrier, the warp sums them out of
+//    shared memory into a staged output row, and lane 0 writes that row back
+//    with one bulk store. Every mbarrier wait has a time and poll budget; a
+//    wait that runs out is counted in g_wait_timeouts and stops the warp.
+//  - grad_return_kernel, for all other cases (mixed types, accumulate mode,
+//    short rows): a warp owns one output row at a time and each lane keeps
+//    U x P 16-byte loads in flight before summing.
+// Both size the grid to whole CTAs per SM and stride over rows in output order.
 #include "cpt_device.cuh"
 #include "cpt_internal.h"
 
@@ -19,6 +29,27 @@ namespace cpt {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kBulkWarps = 2;                 // independent row pipelines per CTA
+constexpr int kBulkMaxSmem = 112 * 1024;      // keeps two CTAs (four warps) on every SM
+
+// Where the bulk-copy kernel beats the 16-byte-load one, from a sweep on
+// GB300 (P = 1..8, rows of 1 to 8 KB, bf16 and float32, 4 GB of writer rows
+// per launch, two passes): it wins by 2 to 9 % from P = 5 up at every row
+// size, for bf16 rows of 2 KB and more at P = 4 and 3 KB and more at P = 3,
+// and for float32 rows up to 2 KB at P = 4. It loses at P = 1 and 2, and by
+// about 20 % wherever its shared memory leaves one CTA per SM.
+__host__ __device__ constexpr bool prefer_bulk(int P, int type, int64_t row_bytes)
+{
+    if (row_bytes < 1024 || (int64_t)kBulkWarps * (P + 1) * row_bytes > kBulkMaxSmem) return false;
+    if (P >= 5) return true;
+    if (P == 4) return type == kBf16 ? row_bytes >= 2048 : row_bytes <= 2048;
+    if (P == 3) return type == kBf16 && row_bytes >= 3072;
+    return false;
+}
+
+// Bulk-copy waits that ran out of their budget (see mbar_wait_bounded); zero
+// unless a copy never completed. Read and reset by read_wait_timeouts.
+__device__ unsigned int g_wait_timeouts;
 
 // Elements of one 16-byte input unit, widened to binary32.
 template <int IN>
@@ -149,9 +180,125 @@ __global__ void __launch_bounds__(kThreads) grad_return_kernel(const GradReturnP
     }
 }
 
+// Same-type overwrite case through shared memory. Per warp: a stage of P
+// input rows and one output row. Lane 0 issues the loads of a row while the
+// map entry of the row after it is already being fetched.
+template <int P, int T>
+__global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const GradReturnParams p)
+{
+    constexpr int E = Unit<T>::kElems;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[kBulkWarps];
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    const int rb = p.in_row_bytes;  // equals out_row_bytes: same element type
+    uint8_t *stage = smem + (size_t)wid * (P + 1) * rb;
+    uint8_t *out = stage + (size_t)P * rb;
+    uint64_t *bar = bars + wid;
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    const int64_t stride = (int64_t)gridDim.x * kBulkWarps;
+    int64_t R = (int64_t)blockIdx.x * kBulkWarps + wid;
+    int64_t g_next = 0;
+    if (lane == 0 && R < p.rows) g_next = __ldg(p.l2g + p.q0 + (R >= p.T ? R - p.T : R));
+    uint32_t phase = 0;
+
+    for (; R < p.rows; R += stride) {
+        const int t = R >= p.T;
+        const int64_t q = p.q0 + (R - t * p.T);
+        const int o = (int)(q / p.Tp);
+        const int64_t j = q - (int64_t)o * p.Tp;
+        if (lane == 0) {
+            const int64_t g = g_next;
+            mbar_expect_tx(bar, (uint32_t)(P * rb));
+#pragma unroll
+            for (int w = 0; w < P; ++w)
+                bulk_load(stage + (size_t)w * rb, (t ? p.w[1][w] : p.w[0][w]) + g * rb, (uint32_t)rb,
+                          bar);
+            const int64_t Rn = R + stride;
+            if (Rn < p.rows) g_next = __ldg(p.l2g + p.q0 + (Rn >= p.T ? Rn - p.T : Rn));
+        }
+        const bool ok = mbar_wait_bounded(bar, phase);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+            if (lane == 0) {
+                atomicAdd(&g_wait_timeouts, 1u);
+                mbar_wait_bounded(bar, phase);  // one more budget for the loads before leaving
+            }
+            break;
+        }
+        phase ^= 1u;
+        if (lane == 0) bulk_wait_read<0>();  // the previous row's store has read `out`
+        __syncwarp();
+        for (int u = lane; u < p.units; u += 32) {
+            float acc[E];
+            Unit<T>::widen(*reinterpret_cast<const uint4 *>(stage + (size_t)u * 16), acc);
+#pragma unroll
+            for (int w = 1; w < P; ++w) {
+                float x[E];
+                Unit<T>::widen(*reinterpret_cast<const uint4 *>(stage + (size_t)w * rb + (size_t)u * 16), x);
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = add_rn(acc[e], x[e]);
+            }
+            uint4 v;
+            if constexpr (T == kBf16) {
+                v = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+            } else {
+                v = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                               __float_as_uint(acc[2]), __float_as_uint(acc[3]));
+            }
+            *reinterpret_cast<uint4 *>(out + (size_t)u * 16) = v;
+        }
+        fence_proxy_async_smem();  // the row's generic writes before the bulk store reads it
+        __syncwarp();
+        if (lane == 0) bulk_store((t ? p.o[1][o] : p.o[0][o]) + j * p.out_row_bytes, out, (uint32_t)rb);
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+}
+
+template <int P, int T>
+cudaError_t launch_bulk(const GradReturnParams &p, size_t smem, cudaStream_t stream)
+{
+    auto kernel = grad_return_bulk_kernel<P, T>;
+    // per device: whether the shared-memory limit is raised, and the
+    // occupancy of the last shared-memory size asked for
+    static bool attr_set[64] = {false};
+    static size_t cached_smem[64] = {0};
+    static int cached_per_sm[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkMaxSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    if (cached_smem[dev] != smem) {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32 * kBulkWarps, smem);
+        if (e != cudaSuccess) return e;
+        cached_per_sm[dev] = per_sm > 0 ? per_sm : 1;
+        cached_smem[dev] = smem;
+    }
+    int64_t blocks = (int64_t)cached_per_sm[dev] * sm_count(dev);
+    const int64_t needed = (p.rows + kBulkWarps - 1) / kBulkWarps;
+    if (blocks > needed) blocks = needed;
+    kernel<<<(unsigned)blocks, 32 * kBulkWarps, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <int P, int IN, int OUT, bool ACC>
 cudaError_t launch_typed(const GradReturnParams &p, cudaStream_t stream)
 {
+    if constexpr (IN == OUT && !ACC) {
+        if (prefer_bulk(P, IN, p.in_row_bytes))
+            return launch_bulk<P, IN>(p, (size_t)kBulkWarps * (P + 1) * p.in_row_bytes, stream);
+    }
     constexpr int U = P <= 4 ? 2 : 1;
     auto kernel = grad_return_kernel<P, IN, OUT, U, ACC>;
     static int blocks_per_sm[64] = {0};  // per device, one table per instantiation
@@ -198,6 +345,16 @@ cudaError_t launch_acc(const GradReturnParams &p, int cp_size, int in, int out, 
 }
 
 }  // namespace
+
+cudaError_t read_wait_timeouts(unsigned int *count, bool reset)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(unsigned int));
+    if (e == cudaSuccess && reset) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
 
 cudaError_t launch_grad_return(const GradReturnParams &p, int cp_size, int in_dtype,
                                int out_dtype, cudaStream_t stream, bool accumulate)

@@ -41,8 +41,10 @@
  *               attempted (as the author's reply in [TE-3235] describes its
  *               size check). On failure nothing is enqueued, the call returns a
  *               non-zero cpt_status and cpt_last_error_string() explains it.
- *               Device-side failures (epoch wait timeout) go to a device
- *               status word. Nothing aborts or traps.
+ *               Device-side failures go to device memory the host reads:
+ *               an epoch wait timeout to a status word, a bulk-copy wait
+ *               that ran out to a counter (cpt_kernel_wait_timeouts).
+ *               Nothing aborts or traps.
  *   Threads     Calls are thread-safe; the error string is per thread.
  *   Graphs      cpt_index_map, cpt_thd_metadata, cpt_thd_real_lengths,
  *               cpt_partition, cpt_restore, cpt_grad_return(_accumulate),
@@ -472,9 +474,26 @@ CPT_API cpt_status cpt_epoch_wait(cpt_epoch *ep, int32_t owner, uint64_t timeout
                           void *stream);
 
 /* Synchronise `stream` and read status[owner] into *device_status.
- * The one blocking call of the library. */
+ * Blocking, like cpt_kernel_wait_timeouts; every other call is
+ * asynchronous. */
 CPT_API cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *stream,
                             int32_t *device_status);
+
+/* Count of bounded waits inside this library's kernels that ran out of
+ * their budget on the current device, since the library was loaded or last
+ * reset (paper has no counterpart: it is this implementation's failure
+ * report). The fused gradient return moves long rows through shared memory
+ * with bulk copies, each completing on an mbarrier. Every wait on one gives
+ * up after about a second or 2^24 polls. A wait that gives up is counted
+ * here, its warp stops, and the output rows it had not reached are left
+ * unwritten. A non-zero count means some output of an earlier call is not
+ * valid.
+ *  count  host, receives the count.
+ *  reset  non-zero: set the count back to zero after reading it.
+ *  Blocking: reads device memory synchronously. Synchronise the streams of
+ *  the calls you want counted first.
+ *  Errors: CPT_ERR_INVALID_ARG (NULL count), CPT_ERR_DEVICE, CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_kernel_wait_timeouts(uint32_t *count, int32_t reset);
 
 /* ------------------------------------------------------------------ */
 /* Ordered slot reduce                                                 */

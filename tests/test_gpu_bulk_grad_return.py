@@ -1,0 +1,136 @@
+"""Parity of the bulk-copy gradient return kernel.
+
+Equal input and output types, overwrite mode and long rows go through the
+kernel that stages the P writer rows in shared memory with bulk copies, where
+it measured faster than the 16-byte-load kernel. These cases aim at it for
+every cp_size from 3 to 8, and at both sides of each edge of where it is
+chosen: the smallest bulk row at P = 3 and P = 4, float32 rows at P = 4, and
+rows at P = 8 just inside and just outside its shared-memory limit. Every
+output is compared bit for bit with the oracle, with canary bands around
+each owner's buffer. The last test checks that no bulk-copy wait ran out of
+its budget in any of them.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from context_attention_token_gb300 import synth
+from gpu_helpers import Guarded, bits, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+DSC, PACKED, PADDED = 0, 1, 3
+
+# (layout, P, document lengths, row elements, element type); the comment
+# names the kernel the library picks for the case
+CASES = [
+    (DSC, 1, [64, 32], 2560, "bf16"),        # 16-byte loads: P = 1
+    (DSC, 2, [40, 24], 2560, "bf16"),        # 16-byte loads: P = 2
+    (DSC, 3, [30, 6, 66], 1536, "bf16"),     # bulk: 3 KB rows, the smallest at P = 3
+    (DSC, 3, [30, 6], 1024, "bf16"),         # 16-byte loads: 2 KB rows at P = 3
+    (DSC, 4, [8, 56, 200], 2560, "bf16"),    # bulk: the pages' 20x128 rows
+    (DSC, 4, [24, 8], 1024, "bf16"),         # bulk: 2 KB rows, the smallest at P = 4
+    (DSC, 4, [24], 504, "bf16"),             # 16-byte loads: 1008-byte rows
+    (DSC, 4, [16, 8], 512, "f32"),           # bulk: 2 KB float32 rows
+    (DSC, 4, [16, 8], 1024, "f32"),          # 16-byte loads: 4 KB float32 rows
+    (DSC, 5, [10, 90], 256, "f32"),          # bulk: 1 KB rows
+    (DSC, 6, [12, 12, 36], 300, "f32"),      # bulk: 1200-byte rows, not a multiple of 512
+    (DSC, 7, [14, 70], 520, "bf16"),         # bulk: 1040-byte rows
+    (DSC, 8, [16, 48, 160], 2560, "bf16"),   # bulk
+    (DSC, 8, [16], 1592, "f32"),             # bulk: 2 x 9 x 6368 B, at the shared-memory limit
+    (DSC, 8, [16], 1596, "f32"),             # 16-byte loads: 16 bytes more per row
+    (PACKED, 3, [5, 50, 17, 3, 9], 1536, "bf16"),
+    (PACKED, 8, [0, 77, 19], 2560, "bf16"),
+    (PADDED, 4, [5, 33, 1, 12], 2560, "bf16"),
+    (PADDED, 8, [3, 17], 1024, "f32"),
+]
+
+
+def _ids(c):
+    return f"L{c[0]}-P{c[1]}-n{len(c[2])}-row{c[3]}-{c[4]}"
+
+
+def _setup(case, seed):
+    layout, P, lens, row, dt = case
+    cu = synth.cu_from_lengths(lens)
+    T = int(cu[-1])
+    if layout == PADDED:
+        cup, l2g, _ = oracle.padded_index_map(P, cu)
+        Tpad = int(cup[-1])
+    else:
+        assert oracle.check_layout(layout, P, cu, T) == 0
+        l2g, _ = oracle.index_map(layout, P, cu, T)
+        Tpad = T
+    rng = np.random.default_rng(seed)
+    gen = synth.uniform_f32 if dt == "f32" else synth.uniform_bf16
+    wk = [gen(rng, (Tpad, row)) for _ in range(P)]
+    wv = [gen(rng, (Tpad, row)) for _ in range(P)]
+    return layout, P, cu, T, Tpad, l2g, wk, wv, (oracle.F32 if dt == "f32" else oracle.BF16)
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_bulk_grad_return_matches_oracle(cpt, cuda_device, case):
+    layout, P, cu, T, Tpad, l2g, wk, wv, code = _setup(case, 7100 + case[1])
+    odt = torch.float32 if case[4] == "f32" else torch.bfloat16
+    row = case[3]
+    plan = cpt.cpt_plan_create(layout, P, cu, T)
+    ok = [Guarded((Tpad // P, row), odt) for _ in range(P)]
+    ov = [Guarded((Tpad // P, row), odt) for _ in range(P)]
+    cpt.cpt_grad_return(plan, torch.stack([to_dev(w) for w in wk]), torch.stack([to_dev(w) for w in wv]),
+                        [o.t for o in ok], [o.t for o in ov])
+    torch.cuda.synchronize()
+    for ws, outs in ((wk, ok), (wv, ov)):
+        want = oracle.grad_return(l2g, ws, code)
+        for o in range(P):
+            assert np.array_equal(bits(to_host(outs[o].t)), bits(want[o])), f"owner {o}"
+            assert outs[o].bands_intact(), f"owner {o}"
+
+
+ROW_RANGE_CASES = [c for c in CASES if c[3] * (4 if c[4] == "f32" else 2) >= 4096]
+
+
+@pytest.mark.parametrize("case", ROW_RANGE_CASES, ids=_ids)
+def test_bulk_grad_return_dk_only_and_row_ranges(cpt, cuda_device, case):
+    """dK alone (no dV pair), then the same sums as three row ranges."""
+    layout, P, cu, T, Tpad, l2g, wk, _wv, code = _setup(case, 7200 + case[1])
+    odt = torch.float32 if case[4] == "f32" else torch.bfloat16
+    row = case[3]
+    plan = cpt.cpt_plan_create(layout, P, cu, T)
+    dkw = torch.stack([to_dev(w) for w in wk])
+    whole = torch.empty((P, Tpad // P, row), dtype=odt, device="cuda")
+    cpt.cpt_grad_return(plan, dkw, None, whole, None)
+    pieces = torch.full((P, Tpad // P, row), 7.0, dtype=odt, device="cuda")
+    cuts = [0, Tpad // 3, (2 * Tpad) // 3 + 1, Tpad]
+    for a, b in zip(cuts, cuts[1:]):
+        cpt.cpt_grad_return_rows(plan, dkw, None, pieces, None, a, b - a)
+    torch.cuda.synchronize()
+    want = oracle.grad_return(l2g, wk, code)
+    got_w, got_p = to_host(whole), to_host(pieces)
+    for o in range(P):
+        assert np.array_equal(bits(got_w[o]), bits(want[o])), f"owner {o}"
+        assert np.array_equal(bits(got_p[o]), bits(want[o])), f"owner {o}"
+
+
+@pytest.mark.parametrize("case", [CASES[4], CASES[17]], ids=_ids)
+def test_bulk_grad_return_noalloc(cpt, cuda_device, case):
+    layout, P, cu, T, Tpad, l2g, wk, wv, code = _setup(case, 7300 + case[1])
+    row = case[3]
+    dkw = torch.stack([to_dev(w) for w in wk])
+    dvw = torch.stack([to_dev(w) for w in wv])
+    dko = torch.empty((P, Tpad // P, row), dtype=torch.bfloat16, device="cuda")
+    dvo = torch.empty_like(dko)
+    cpt.cpt_grad_return_noalloc(layout, P, cu, T, dkw, dvw, dko, dvo)
+    torch.cuda.synchronize()
+    for ws, out in ((wk, dko), (wv, dvo)):
+        want = oracle.grad_return(l2g, ws, code)
+        got = to_host(out)
+        for o in range(P):
+            assert np.array_equal(got[o], want[o]), f"owner {o}"
+
+
+def test_no_bulk_copy_wait_ran_out(cpt, cuda_device):
+    """Every bulk-copy wait above completed within its budget."""
+    torch.cuda.synchronize()
+    assert cpt.cpt_kernel_wait_timeouts() == 0
+    assert cpt.cpt_kernel_wait_timeouts(reset=True) == 0
