@@ -427,6 +427,8 @@ def run_gpu(args):
         dist.barrier()
     from context_attention_token_gb300 import cpt, synth
 
+    cpt.cpt_set_grad_return_kernel({"auto": cpt.CPT_GRAD_RETURN_AUTO, "loads": cpt.CPT_GRAD_RETURN_LOADS,
+                                    "bulk": cpt.CPT_GRAD_RETURN_BULK}[args.grad_return_kernel])
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
 
@@ -647,6 +649,7 @@ def run_gpu(args):
         "data": "synthetic (seeded device N(0,1) Q/K/V, N(0,0.02) dK/dV)",
         "config": {"workload": workload(), "P": P, "S": S, "H": H, "D": D,
                    "layout": "dual_chunk_swap", "grad_return_path": PATH,
+                   "grad_return_kernel": args.grad_return_kernel,
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (21.5 GB touched per step), no flush",
                    "step_bytes": step_bytes(S)},
@@ -813,6 +816,12 @@ def run_next_rows(args):
                 lambda: cpt.cpt_grad_return_noalloc(0, Pw, [0, S], S, dkw, dvw, dko, dvo), stream)
             emit("grad_return_noalloc_P4", ms, S * (2 * (Pw + 1) * row + 2 * 4) + S * 4, P=Pw, S=S,
                  note="includes its own map build (index-map kernel) each call")
+            for kname, kcode in (("loads", cpt.CPT_GRAD_RETURN_LOADS), ("bulk", cpt.CPT_GRAD_RETURN_BULK)):
+                cpt.cpt_set_grad_return_kernel(kcode)
+                ms = _median_launch_ms(lambda: cpt.cpt_grad_return(planp, dkw, dvw, dko, dvo), stream)
+                emit(f"grad_return_P4_{kname}_kernel", ms, S * (2 * (Pw + 1) * row + 2 * 4), P=Pw, S=S,
+                     kernel=kname)
+            cpt.cpt_set_grad_return_kernel(cpt.CPT_GRAD_RETURN_AUTO)
         del dkw, dvw, dko, dvo
         torch.cuda.empty_cache()
 
@@ -832,19 +841,23 @@ def run_next_rows(args):
         wv = synth.device_normal_bf16((P, Tg, Hg, D), 6401, 1.0, "cuda")
         ok = torch.empty((P, Tg // P, Hg, D), dtype=torch.bfloat16, device="cuda")
         ov = torch.empty_like(ok)
-        evs = []
-        for it in range(23):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            cpt.cpt_grad_return(plg, wk, wv, ok, ov)
-            b.record(stream)
-            if it >= 3:
-                evs.append((a, b))
-        torch.cuda.synchronize()
-        ms = statistics.median(x.elapsed_time(y) for x, y in evs)
-        emit(name, ms, Tg * (2 * (P + 1) * Hg * D * 2 + 2 * 4), P=P, T=Tg, docs=len(lens_g),
-             l2="flushed before each launch")
+        for kname, kcode in (("", cpt.CPT_GRAD_RETURN_AUTO), ("_loads_kernel", cpt.CPT_GRAD_RETURN_LOADS),
+                             ("_bulk_kernel", cpt.CPT_GRAD_RETURN_BULK)):
+            cpt.cpt_set_grad_return_kernel(kcode)
+            evs = []
+            for it in range(23):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                cpt.cpt_grad_return(plg, wk, wv, ok, ov)
+                b.record(stream)
+                if it >= 3:
+                    evs.append((a, b))
+            torch.cuda.synchronize()
+            ms = statistics.median(x.elapsed_time(y) for x, y in evs)
+            emit(name + kname, ms, Tg * (2 * (P + 1) * Hg * D * 2 + 2 * 4), P=P, T=Tg, docs=len(lens_g),
+                 l2="flushed before each launch", kernel=kname.strip("_").replace("_kernel", "") or "auto")
+        cpt.cpt_set_grad_return_kernel(cpt.CPT_GRAD_RETURN_AUTO)
         del wk, wv, ok, ov
         torch.cuda.empty_cache()
     del flush
@@ -1051,6 +1064,9 @@ def main():
     ap.add_argument("--sweep", choices=["slot_reduce", "host_link"], default=None,
                     help="instead of the step: the slot-reduce message-size sweep, or the "
                          "host link's copy rates")
+    ap.add_argument("--grad-return-kernel", choices=["auto", "loads", "bulk"], default="auto",
+                    help="kernel of the fused gradient return: the measured rule (default), or one "
+                         "forced")
     ap.add_argument("--tokens", type=int, default=S, help="S (multiple of 2P)")
     ap.add_argument("--heads", type=int, default=H)
     args = ap.parse_args()

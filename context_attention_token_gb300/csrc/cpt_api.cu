@@ -997,6 +997,15 @@ cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *stream, in
     return CPT_OK;
 }
 
+cpt_status cpt_set_grad_return_kernel(cpt_grad_return_kernel kernel)
+{
+    Trace trace("cpt_set_grad_return_kernel");
+    if (kernel != CPT_GRAD_RETURN_AUTO && kernel != CPT_GRAD_RETURN_LOADS && kernel != CPT_GRAD_RETURN_BULK)
+        return fail(CPT_ERR_INVALID_ARG, "unknown gradient return kernel %d", (int)kernel);
+    set_grad_return_kernel((int)kernel);
+    return CPT_OK;
+}
+
 cpt_status cpt_kernel_wait_timeouts(uint32_t *count, int32_t reset)
 {
     Trace trace("cpt_kernel_wait_timeouts");

@@ -68,6 +68,10 @@ struct GradReturnParams {
     int32_t in_row_bytes;
     int32_t out_row_bytes;
 };
+// Kernel of the fused gradient return: 0 = the measured rule, 1 = 16-byte
+// loads, 2 = bulk copies wherever they can run. Process-wide.
+void set_grad_return_kernel(int choice);
+
 // Reads (and, if reset, zeroes) the count of bulk-copy waits in the gradient
 // return kernel that ran out of their budget, on the current device.
 // Synchronous.

@@ -10,8 +10,9 @@
 // HBM-bound: per output row it reads P input rows and writes one. Two kernels
 // share the arithmetic (binary32 adds in writer order):
 //  - grad_return_bulk_kernel, for equal input and output types, overwrite,
-//    and the cp_size / row sizes where it measured faster (prefer_bulk): every
-//    warp runs its own row pipeline.
+//    and the cp_size, row and launch sizes where it measured faster
+//    (prefer_bulk; set_grad_return_kernel overrides): every warp runs its own
+//    row pipeline.
 //    Lane 0 brings the P writer rows into shared memory with P bulk copies
 //    (cp.async.bulk) counted on one mbarrier, the warp sums them out of
 //    shared memory into a staged output row, and lane 0 writes that row back
@@ -21,6 +22,8 @@
 //    short rows): a warp owns one output row at a time and each lane keeps
 //    U x P 16-byte loads in flight before summing.
 // Both size the grid to whole CTAs per SM and stride over rows in output order.
+#include <atomic>
+
 #include "cpt_device.cuh"
 #include "cpt_internal.h"
 
@@ -38,14 +41,33 @@ constexpr int kBulkMaxSmem = 112 * 1024;      // keeps two CTAs (four warps) on 
 // size, for bf16 rows of 2 KB and more at P = 4 and 3 KB and more at P = 3,
 // and for float32 rows up to 2 KB at P = 4. It loses at P = 1 and 2, and by
 // about 20 % wherever its shared memory leaves one CTA per SM.
-__host__ __device__ constexpr bool prefer_bulk(int P, int type, int64_t row_bytes)
+//
+// With L2 flushed before every launch (as after an attention backward that
+// has just written the writer rows), the bulk kernel also starts more slowly:
+// at P = 4 and 6 it lost 1-7 % on launches of 0.17 to 1.3 GB and won from
+// about 2.7 GB (P = 4: even at 2.7 GB, -1 to -2 % at 5.4 GB; P = 6: -1.5 %
+// at 2.7 GB, -4.5 % at 5.4 GB), while at P = 8 it won at almost every size.
+// So for P <= 6 the rule also asks for launches of at least 2 GiB.
+constexpr int64_t kBulkMinLaunchBytes = int64_t(2) << 30;
+
+bool bulk_fits(int P, int64_t row_bytes)
 {
-    if (row_bytes < 1024 || (int64_t)kBulkWarps * (P + 1) * row_bytes > kBulkMaxSmem) return false;
+    return (int64_t)kBulkWarps * (P + 1) * row_bytes <= kBulkMaxSmem;
+}
+
+bool prefer_bulk(int P, int type, int64_t row_bytes, int64_t launch_bytes)
+{
+    if (row_bytes < 1024 || !bulk_fits(P, row_bytes)) return false;
+    if (P <= 6 && launch_bytes < kBulkMinLaunchBytes) return false;
     if (P >= 5) return true;
     if (P == 4) return type == kBf16 ? row_bytes >= 2048 : row_bytes <= 2048;
     if (P == 3) return type == kBf16 && row_bytes >= 3072;
     return false;
 }
+
+// 0 = the measured rule, 1 = always the 16-byte-load kernel, 2 = the bulk
+// kernel wherever it can run (set_grad_return_kernel).
+std::atomic<int> g_kernel_choice{0};
 
 // Bulk-copy waits that ran out of their budget (see mbar_wait_bounded); zero
 // unless a copy never completed. Read and reset by read_wait_timeouts.
@@ -296,8 +318,11 @@ template <int P, int IN, int OUT, bool ACC>
 cudaError_t launch_typed(const GradReturnParams &p, cudaStream_t stream)
 {
     if constexpr (IN == OUT && !ACC) {
-        if (prefer_bulk(P, IN, p.in_row_bytes))
-            return launch_bulk<P, IN>(p, (size_t)kBulkWarps * (P + 1) * p.in_row_bytes, stream);
+        const int choice = g_kernel_choice.load(std::memory_order_relaxed);
+        const int64_t launch_bytes = p.rows * (P + 1) * (int64_t)p.in_row_bytes;
+        const bool bulk = choice == 2 ? bulk_fits(P, p.in_row_bytes)
+                                      : choice == 0 && prefer_bulk(P, IN, p.in_row_bytes, launch_bytes);
+        if (bulk) return launch_bulk<P, IN>(p, (size_t)kBulkWarps * (P + 1) * p.in_row_bytes, stream);
     }
     constexpr int U = P <= 4 ? 2 : 1;
     auto kernel = grad_return_kernel<P, IN, OUT, U, ACC>;
@@ -345,6 +370,11 @@ cudaError_t launch_acc(const GradReturnParams &p, int cp_size, int in, int out, 
 }
 
 }  // namespace
+
+void set_grad_return_kernel(int choice)
+{
+    g_kernel_choice.store(choice, std::memory_order_relaxed);
+}
 
 cudaError_t read_wait_timeouts(unsigned int *count, bool reset)
 {

@@ -135,6 +135,13 @@ typedef enum cpt_dtype { CPT_F32 = 0, CPT_BF16 = 1 } cpt_dtype;
  *           writer's publish of this epoch is already enqueued. */
 typedef enum cpt_wait_mode { CPT_WAIT_BOUNDED = 0, CPT_WAIT_DRIVER = 1 } cpt_wait_mode;
 
+/* Which kernel the fused gradient return runs (cpt_set_grad_return_kernel). */
+typedef enum cpt_grad_return_kernel {
+    CPT_GRAD_RETURN_AUTO = 0,  /* the measured rule (default) */
+    CPT_GRAD_RETURN_LOADS = 1, /* 16-byte loads into registers */
+    CPT_GRAD_RETURN_BULK = 2   /* bulk copies through shared memory, where it can run */
+} cpt_grad_return_kernel;
+
 typedef struct cpt_plan cpt_plan;   /* opaque: layout, P, T, pointers into the workspace */
 typedef struct cpt_epoch cpt_epoch; /* opaque: epoch counter and publish bookkeeping    */
 
@@ -362,6 +369,29 @@ CPT_API cpt_status cpt_grad_return_accumulate(const cpt_plan *plan, const void *
                                               void *const *dk_owners, void *const *dv_owners,
                                               int64_t row_elems, cpt_dtype in, cpt_dtype out,
                                               void *stream);
+
+/* Choose the kernel of cpt_grad_return, cpt_grad_return_rows and
+ * cpt_grad_return_noalloc, for the whole process and every device (paper has
+ * no counterpart: a tuning and testing control of this implementation).
+ * Both kernels compute the same bits.
+ *  - CPT_GRAD_RETURN_LOADS: each lane keeps P 16-byte loads per row unit
+ *    in flight in registers. Every case can run it.
+ *  - CPT_GRAD_RETURN_BULK: each warp stages one owner row's P writer rows
+ *    in shared memory with bulk copies and stores the sum with one bulk
+ *    copy. It needs equal input and output types, overwrite mode (not
+ *    cpt_grad_return_accumulate) and 2 x (P+1) x row bytes of at most
+ *    112 KB. Where these do not hold, the loads kernel runs.
+ *  - CPT_GRAD_RETURN_AUTO (the default): bulk where it measured faster on
+ *    GB300, loads elsewhere. The measured rule asks for rows of at least
+ *    1 KB, and for P <= 6 launches of at least 2 GiB. Per P:
+ *      P >= 5: any row size;
+ *      P = 4:  bf16 rows of at least 2 KB, float32 rows of at most 2 KB;
+ *      P = 3:  bf16 rows of at least 3 KB;
+ *      P <= 2: never.
+ *  The choice applies to calls made after this one returns. Concurrent
+ *  calls from other threads see either the old or the new choice.
+ *  Errors: CPT_ERR_INVALID_ARG (not one of the three values). */
+CPT_API cpt_status cpt_set_grad_return_kernel(cpt_grad_return_kernel kernel);
 
 /* Largest batch cpt_grad_return_noalloc accepts. */
 #define CPT_NOALLOC_MAX_TOKENS 1048576

@@ -1,11 +1,13 @@
 """Parity of the bulk-copy gradient return kernel.
 
-Equal input and output types, overwrite mode and long rows go through the
-kernel that stages the P writer rows in shared memory with bulk copies, where
-it measured faster than the 16-byte-load kernel. These cases aim at it for
-every cp_size from 3 to 8, and at both sides of each edge of where it is
-chosen: the smallest bulk row at P = 3 and P = 4, float32 rows at P = 4, and
-rows at P = 8 just inside and just outside its shared-memory limit. Every
+With equal input and output types and overwrite mode, the gradient return
+can run either of two kernels: 16-byte loads into registers, or bulk copies
+that stage the P writer rows in shared memory. Each case here runs three
+times: under the measured rule, and with each kernel forced. The cases span
+every cp_size and both sides of each edge of the rule: the smallest bulk row
+at P = 3 and P = 4, float32 rows at P = 4, and rows at P = 8 just inside and
+just outside the bulk kernel's shared-memory limit (outside it, forcing bulk
+runs the loads kernel). Every
 output is compared bit for bit with the oracle, with canary bands around
 each owner's buffer. The last test checks that no bulk-copy wait ran out of
 its budget in any of them.
@@ -47,6 +49,19 @@ CASES = [
 ]
 
 
+KERNELS = ["auto", "loads", "bulk"]
+
+
+@pytest.fixture
+def kernel(cpt, request):
+    """Run the test with the requested kernel choice, then restore the default."""
+    code = {"auto": cpt.CPT_GRAD_RETURN_AUTO, "loads": cpt.CPT_GRAD_RETURN_LOADS,
+            "bulk": cpt.CPT_GRAD_RETURN_BULK}[request.param]
+    cpt.cpt_set_grad_return_kernel(code)
+    yield request.param
+    cpt.cpt_set_grad_return_kernel(cpt.CPT_GRAD_RETURN_AUTO)
+
+
 def _ids(c):
     return f"L{c[0]}-P{c[1]}-n{len(c[2])}-row{c[3]}-{c[4]}"
 
@@ -69,8 +84,9 @@ def _setup(case, seed):
     return layout, P, cu, T, Tpad, l2g, wk, wv, (oracle.F32 if dt == "f32" else oracle.BF16)
 
 
+@pytest.mark.parametrize("kernel", KERNELS, indirect=True)
 @pytest.mark.parametrize("case", CASES, ids=_ids)
-def test_bulk_grad_return_matches_oracle(cpt, cuda_device, case):
+def test_bulk_grad_return_matches_oracle(cpt, cuda_device, case, kernel):
     layout, P, cu, T, Tpad, l2g, wk, wv, code = _setup(case, 7100 + case[1])
     odt = torch.float32 if case[4] == "f32" else torch.bfloat16
     row = case[3]
@@ -90,8 +106,9 @@ def test_bulk_grad_return_matches_oracle(cpt, cuda_device, case):
 ROW_RANGE_CASES = [c for c in CASES if c[3] * (4 if c[4] == "f32" else 2) >= 4096]
 
 
+@pytest.mark.parametrize("kernel", KERNELS, indirect=True)
 @pytest.mark.parametrize("case", ROW_RANGE_CASES, ids=_ids)
-def test_bulk_grad_return_dk_only_and_row_ranges(cpt, cuda_device, case):
+def test_bulk_grad_return_dk_only_and_row_ranges(cpt, cuda_device, case, kernel):
     """dK alone (no dV pair), then the same sums as three row ranges."""
     layout, P, cu, T, Tpad, l2g, wk, _wv, code = _setup(case, 7200 + case[1])
     odt = torch.float32 if case[4] == "f32" else torch.bfloat16
@@ -112,8 +129,9 @@ def test_bulk_grad_return_dk_only_and_row_ranges(cpt, cuda_device, case):
         assert np.array_equal(bits(got_p[o]), bits(want[o])), f"owner {o}"
 
 
+@pytest.mark.parametrize("kernel", ["loads", "bulk"], indirect=True)
 @pytest.mark.parametrize("case", [CASES[4], CASES[17]], ids=_ids)
-def test_bulk_grad_return_noalloc(cpt, cuda_device, case):
+def test_bulk_grad_return_noalloc(cpt, cuda_device, case, kernel):
     layout, P, cu, T, Tpad, l2g, wk, wv, code = _setup(case, 7300 + case[1])
     row = case[3]
     dkw = torch.stack([to_dev(w) for w in wk])
