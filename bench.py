@@ -427,8 +427,8 @@ def run_gpu(args):
         dist.barrier()
     from context_attention_token_gb300 import cpt, synth
 
-    cpt.cpt_set_grad_return_kernel({"auto": cpt.CPT_GRAD_RETURN_AUTO, "loads": cpt.CPT_GRAD_RETURN_LOADS,
-                                    "bulk": cpt.CPT_GRAD_RETURN_BULK}[args.grad_return_kernel])
+    cpt.cpt_set_sum_kernel({"auto": cpt.CPT_SUM_KERNEL_AUTO, "loads": cpt.CPT_SUM_KERNEL_LOADS,
+                                    "bulk": cpt.CPT_SUM_KERNEL_BULK}[args.sum_kernel])
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
 
@@ -649,7 +649,7 @@ def run_gpu(args):
         "data": "synthetic (seeded device N(0,1) Q/K/V, N(0,0.02) dK/dV)",
         "config": {"workload": workload(), "P": P, "S": S, "H": H, "D": D,
                    "layout": "dual_chunk_swap", "grad_return_path": PATH,
-                   "grad_return_kernel": args.grad_return_kernel,
+                   "sum_kernel": args.sum_kernel,
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (21.5 GB touched per step), no flush",
                    "step_bytes": step_bytes(S)},
@@ -816,12 +816,12 @@ def run_next_rows(args):
                 lambda: cpt.cpt_grad_return_noalloc(0, Pw, [0, S], S, dkw, dvw, dko, dvo), stream)
             emit("grad_return_noalloc_P4", ms, S * (2 * (Pw + 1) * row + 2 * 4) + S * 4, P=Pw, S=S,
                  note="includes its own map build (index-map kernel) each call")
-            for kname, kcode in (("loads", cpt.CPT_GRAD_RETURN_LOADS), ("bulk", cpt.CPT_GRAD_RETURN_BULK)):
-                cpt.cpt_set_grad_return_kernel(kcode)
+            for kname, kcode in (("loads", cpt.CPT_SUM_KERNEL_LOADS), ("bulk", cpt.CPT_SUM_KERNEL_BULK)):
+                cpt.cpt_set_sum_kernel(kcode)
                 ms = _median_launch_ms(lambda: cpt.cpt_grad_return(planp, dkw, dvw, dko, dvo), stream)
                 emit(f"grad_return_P4_{kname}_kernel", ms, S * (2 * (Pw + 1) * row + 2 * 4), P=Pw, S=S,
                      kernel=kname)
-            cpt.cpt_set_grad_return_kernel(cpt.CPT_GRAD_RETURN_AUTO)
+            cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO)
         del dkw, dvw, dko, dvo
         torch.cuda.empty_cache()
 
@@ -841,9 +841,9 @@ def run_next_rows(args):
         wv = synth.device_normal_bf16((P, Tg, Hg, D), 6401, 1.0, "cuda")
         ok = torch.empty((P, Tg // P, Hg, D), dtype=torch.bfloat16, device="cuda")
         ov = torch.empty_like(ok)
-        for kname, kcode in (("", cpt.CPT_GRAD_RETURN_AUTO), ("_loads_kernel", cpt.CPT_GRAD_RETURN_LOADS),
-                             ("_bulk_kernel", cpt.CPT_GRAD_RETURN_BULK)):
-            cpt.cpt_set_grad_return_kernel(kcode)
+        for kname, kcode in (("", cpt.CPT_SUM_KERNEL_AUTO), ("_loads_kernel", cpt.CPT_SUM_KERNEL_LOADS),
+                             ("_bulk_kernel", cpt.CPT_SUM_KERNEL_BULK)):
+            cpt.cpt_set_sum_kernel(kcode)
             evs = []
             for it in range(23):
                 flush.zero_()
@@ -857,7 +857,7 @@ def run_next_rows(args):
             ms = statistics.median(x.elapsed_time(y) for x, y in evs)
             emit(name + kname, ms, Tg * (2 * (P + 1) * Hg * D * 2 + 2 * 4), P=P, T=Tg, docs=len(lens_g),
                  l2="flushed before each launch", kernel=kname.strip("_").replace("_kernel", "") or "auto")
-        cpt.cpt_set_grad_return_kernel(cpt.CPT_GRAD_RETURN_AUTO)
+        cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO)
         del wk, wv, ok, ov
         torch.cuda.empty_cache()
     del flush
@@ -948,10 +948,10 @@ def run_host_link_sweep(args):
 
 
 def run_slot_reduce_sweep(args):
-    """P=8 slot buffers of N bytes each, N = 1 KB x 4^k up to 1 GB, float32 and
+    """P slot buffers (--slots, default 8) of N bytes each, N = 1 KB x 4^k up to 1 GB, float32 and
     bf16: one ordered sum per launch. One JSON line per (dtype, N), with the
     launch latency (back-to-back C-ABI calls, and replays of a CUDA graph of
-    such calls) and the effective bandwidth over 9N algorithmic bytes."""
+    such calls) and the effective bandwidth over (P+1)N algorithmic bytes."""
     import torch
 
     from context_attention_token_gb300 import build as cpt_build
@@ -960,10 +960,12 @@ def run_slot_reduce_sweep(args):
     from context_attention_token_gb300 import cpt
 
     torch.cuda.set_device(0)
+    cpt.cpt_set_sum_kernel({"auto": cpt.CPT_SUM_KERNEL_AUTO, "loads": cpt.CPT_SUM_KERNEL_LOADS,
+                            "bulk": cpt.CPT_SUM_KERNEL_BULK}[args.sum_kernel])
     peak, peak_src = load_peak()
     stream = torch.cuda.Stream()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
-    n_slots = 8
+    n_slots = args.slots
     for dtype in (torch.float32, torch.bfloat16):
         esz = torch.tensor([], dtype=dtype).element_size()
         for k in range(11):
@@ -973,7 +975,7 @@ def run_slot_reduce_sweep(args):
             gen.manual_seed(5000 + k)
             slots = [(torch.rand(n, device="cuda", generator=gen) * 2 - 1).to(dtype) for _ in range(n_slots)]
             dst = torch.empty(n, dtype=dtype, device="cuda")
-            iters = max(3, min(2000, int(2e9 // (9 * nbytes))))
+            iters = max(3, min(2000, int(2e9 // ((n_slots + 1) * nbytes))))
             torch.cuda.synchronize()
             with torch.cuda.stream(stream):
                 for _ in range(3):
@@ -1017,13 +1019,14 @@ def run_slot_reduce_sweep(args):
                     cold.append((a3, b3))
             torch.cuda.synchronize()
             cold_us = statistics.median(a3.elapsed_time(b3) for a3, b3 in cold) * 1e3
-            gbs = 9 * nbytes / (cold_us * 1e-6) / 1e9
+            gbs = (n_slots + 1) * nbytes / (cold_us * 1e-6) / 1e9
             line = {"sweep": "slot_reduce", "metric": "slot_reduce latency and effective GB/s",
                     "dtype": "f32" if dtype == torch.float32 else "bf16", "slots": n_slots,
+                    "sum_kernel": args.sum_kernel,
                     "bytes_per_slot": nbytes, "iters": iters,
                     "us_per_call_launched": call_us, "us_per_call_graph": graph_us,
                     "us_per_call_cold_l2": cold_us,
-                    "l2_resident_when_repeated": 9 * nbytes < 129 * 2**20,
+                    "l2_resident_when_repeated": (n_slots + 1) * nbytes < 129 * 2**20,
                     "gbs": gbs, "frac_of_peak": gbs / peak, "peak": peak, "peak_source": peak_src}
             print(json.dumps(line), flush=True)
             del slots, dst
@@ -1064,9 +1067,10 @@ def main():
     ap.add_argument("--sweep", choices=["slot_reduce", "host_link"], default=None,
                     help="instead of the step: the slot-reduce message-size sweep, or the "
                          "host link's copy rates")
-    ap.add_argument("--grad-return-kernel", choices=["auto", "loads", "bulk"], default="auto",
-                    help="kernel of the fused gradient return: the measured rule (default), or one "
-                         "forced")
+    ap.add_argument("--sum-kernel", choices=["auto", "loads", "bulk"], default="auto",
+                    help="kernel of the gradient return and the slot reduce: the measured rule "
+                         "(default), or one forced")
+    ap.add_argument("--slots", type=int, default=8, help="--sweep slot_reduce: number of slots (1..8)")
     ap.add_argument("--tokens", type=int, default=S, help="S (multiple of 2P)")
     ap.add_argument("--heads", type=int, default=H)
     args = ap.parse_args()

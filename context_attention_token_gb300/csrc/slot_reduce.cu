@@ -9,9 +9,16 @@
 // the P contributions are P buffers in one HBM; dst[i] is their binary32 sum in
 // slot order, starting from slot 0's value, rounded once.
 //
-// Small messages are launch-latency-bound; large ones are HBM-bound: each
-// thread keeps U x P 16-byte loads in flight; the grid never exceeds what is
-// resident at once, and a grid-stride loop covers the rest.
+// Small messages are launch-latency-bound; large ones are HBM-bound. Two
+// kernels share the arithmetic:
+//  - slot_reduce_kernel: each thread keeps U x P 16-byte loads in flight; the
+//    grid never exceeds what is resident at once, and a grid-stride loop
+//    covers the rest. It handles every case and the ragged tail.
+//  - slot_reduce_bulk_kernel (equal input and output types): each warp moves
+//    kChunk bytes of every slot into shared memory with P bulk copies on one
+//    mbarrier, sums them there, and writes the chunk back with one bulk store.
+//    Whole chunks only; the rest goes to slot_reduce_kernel. Every mbarrier
+//    wait has a budget; one that runs out is counted in g_wait_timeouts.
 #include "cpt_device.cuh"
 #include "cpt_internal.h"
 
@@ -20,6 +27,13 @@ namespace cpt {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kBulkWarps = 2;      // independent chunk pipelines per CTA
+constexpr int kChunk = 4096;       // bytes of every slot per warp step
+constexpr int kBulkMaxSmem = 112 * 1024;
+
+// Bulk-copy waits that ran out of their budget; zero unless a copy never
+// completed. Read by read_slot_reduce_wait_timeouts.
+__device__ unsigned int g_wait_timeouts;
 
 template <int IN>
 __device__ __forceinline__ float load_scalar(const uint8_t *base, int64_t i)
@@ -119,8 +133,141 @@ __global__ void __launch_bounds__(kThreads, 4) slot_reduce_kernel(const SlotRedu
     }
 }
 
+// dst chunk c = ordered sum of chunk c of every slot, chunks of kChunk bytes,
+// equal input and output types.
+template <int P, int T>
+__global__ void __launch_bounds__(32 * kBulkWarps) slot_reduce_bulk_kernel(const SlotReduceParams p,
+                                                                         const int64_t n_chunks)
+{
+    if (p.status != nullptr && *reinterpret_cast<const volatile int32_t *>(p.status) != 0) return;
+    constexpr int E = T == kBf16 ? 8 : 4;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[kBulkWarps];
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    uint8_t *stage = smem + (size_t)wid * (P + 1) * kChunk;
+    uint8_t *out = stage + (size_t)P * kChunk;
+    uint64_t *bar = bars + wid;
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    uint32_t phase = 0;
+    const int64_t stride = (int64_t)gridDim.x * kBulkWarps;
+    for (int64_t c = (int64_t)blockIdx.x * kBulkWarps + wid; c < n_chunks; c += stride) {
+        if (lane == 0) {
+            mbar_expect_tx(bar, (uint32_t)(P * kChunk));
+#pragma unroll
+            for (int w = 0; w < P; ++w) bulk_load(stage + (size_t)w * kChunk, p.s[w] + c * kChunk, kChunk, bar);
+        }
+        const bool ok = mbar_wait_bounded(bar, phase);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+            if (lane == 0) {
+                atomicAdd(&g_wait_timeouts, 1u);
+                mbar_wait_bounded(bar, phase);  // one more budget for the loads before leaving
+            }
+            break;
+        }
+        phase ^= 1u;
+        if (lane == 0) bulk_wait_read<0>();  // the previous chunk's store has read `out`
+        __syncwarp();
+        for (int u = lane; u < kChunk / 16; u += 32) {
+            float acc[E], x[E];
+            const uint4 v0 = *reinterpret_cast<const uint4 *>(stage + (size_t)u * 16);
+            if constexpr (T == kBf16) widen<T>(v0, acc); else widen_f32(v0, acc);
+#pragma unroll
+            for (int w = 1; w < P; ++w) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(stage + (size_t)w * kChunk + (size_t)u * 16);
+                if constexpr (T == kBf16) widen<T>(v, x); else widen_f32(v, x);
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = add_rn(acc[e], x[e]);
+            }
+            uint4 r;
+            if constexpr (T == kBf16) {
+                r = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+            } else {
+                r = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                               __float_as_uint(acc[3]));
+            }
+            *reinterpret_cast<uint4 *>(out + (size_t)u * 16) = r;
+        }
+        fence_proxy_async_smem();  // the chunk's generic writes before the bulk store reads it
+        __syncwarp();
+        if (lane == 0) bulk_store(p.dst + c * kChunk, out, kChunk);
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+}
+
+template <int P, int T>
+cudaError_t launch_bulk(const SlotReduceParams &p, int64_t n_chunks, cudaStream_t stream)
+{
+    auto kernel = slot_reduce_bulk_kernel<P, T>;
+    constexpr size_t smem = (size_t)kBulkWarps * (P + 1) * kChunk;
+    static int blocks_per_sm[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (blocks_per_sm[dev] == 0) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 32 * kBulkWarps, smem);
+        if (e != cudaSuccess) return e;
+        blocks_per_sm[dev] = n > 0 ? n : 1;
+    }
+    int64_t blocks = (int64_t)blocks_per_sm[dev] * sm_count(dev);
+    const int64_t needed = (n_chunks + kBulkWarps - 1) / kBulkWarps;
+    if (blocks > needed) blocks = needed;
+    kernel<<<(unsigned)blocks, 32 * kBulkWarps, smem, stream>>>(p, n_chunks);
+    return cudaGetLastError();
+}
+
+// Whether the bulk kernel takes the whole chunks of this call (choice: 0 =
+// measured rule, 1 = never, 2 = wherever it can run). The rule comes from the
+// slot-reduce sweep on GB300 (2, 4 and 8 slots, 1 KB to 1 GB per slot, both
+// kernels): right after an L2 flush the bulk kernel was 2-5 % faster at 1 GB
+// per slot, even at 256 MB, and slower below (by up to 30 % on small, warm,
+// back-to-back calls, where its one-chunk-per-warp pipeline shows).
+constexpr int64_t kBulkMinSlotBytes = int64_t(1) << 30;
+
+bool use_bulk(int choice, int P, int64_t bytes_per_slot)
+{
+    if ((int64_t)kBulkWarps * (P + 1) * kChunk > kBulkMaxSmem || bytes_per_slot < kChunk) return false;
+    if (choice == 2) return true;
+    return choice == 0 && bytes_per_slot >= kBulkMinSlotBytes;
+}
+
+template <int P, int IN, int OUT>
+cudaError_t launch_loads(const SlotReduceParams &p, cudaStream_t stream);
+
 template <int P, int IN, int OUT>
 cudaError_t launch_typed(const SlotReduceParams &p, cudaStream_t stream)
+{
+    if constexpr (IN == OUT) {
+        constexpr int esz = IN == kBf16 ? 2 : 4;
+        const int64_t bytes = p.n_elems * esz;
+        if (use_bulk(sum_kernel(), P, bytes)) {
+            const int64_t n_chunks = bytes / kChunk;
+            cudaError_t e = launch_bulk<P, IN>(p, n_chunks, stream);
+            if (e != cudaSuccess) return e;
+            const int64_t done = n_chunks * kChunk;
+            if (done == bytes) return cudaSuccess;
+            SlotReduceParams rest = p;  // the tail after the whole chunks
+            for (int w = 0; w < P; ++w) rest.s[w] = p.s[w] + done;
+            rest.dst = p.dst + done;
+            rest.n_elems = p.n_elems - done / esz;
+            return launch_loads<P, IN, OUT>(rest, stream);
+        }
+    }
+    return launch_loads<P, IN, OUT>(p, stream);
+}
+
+template <int P, int IN, int OUT>
+cudaError_t launch_loads(const SlotReduceParams &p, cudaStream_t stream)
 {
     constexpr int U = P <= 4 ? 2 : 1;
     constexpr int E = IN == kBf16 ? 8 : 4;
@@ -152,13 +299,6 @@ cudaError_t launch_p(const SlotReduceParams &p, int in, int out, cudaStream_t s)
     if (in == kBf16 && out == kF32) return launch_typed<P, kBf16, kF32>(p, s);
     if (in == kF32 && out == kBf16) return launch_typed<P, kF32, kBf16>(p, s);
     return launch_typed<P, kF32, kF32>(p, s);
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
@@ -194,6 +334,16 @@ __global__ void epoch_check_kernel(const uint32_t *flags_row, int P, uint32_t ep
 }
 
 }  // namespace
+
+cudaError_t read_slot_reduce_wait_timeouts(unsigned int *count, bool reset)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(unsigned int));
+    if (e == cudaSuccess && reset) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
 
 cudaError_t launch_slot_reduce(const SlotReduceParams &p, int n_slots, int in_dtype,
                                int out_dtype, cudaStream_t stream)

@@ -155,10 +155,10 @@ def test_binding_constants_match_header(cpt):
         assert getattr(cpt, name) == val, name
 
 
-def test_grad_return_kernel_choice_validated(cpt):
+def test_sum_kernel_choice_validated(cpt):
     """The kernel choice takes the three enumerators and refuses anything else."""
     for bad in (-1, 3, 99):
         with pytest.raises(cpt.CptError):
-            cpt.cpt_set_grad_return_kernel(bad)
-    for k in (cpt.CPT_GRAD_RETURN_LOADS, cpt.CPT_GRAD_RETURN_BULK, cpt.CPT_GRAD_RETURN_AUTO):
-        cpt.cpt_set_grad_return_kernel(k)
+            cpt.cpt_set_sum_kernel(bad)
+    for k in (cpt.CPT_SUM_KERNEL_LOADS, cpt.CPT_SUM_KERNEL_BULK, cpt.CPT_SUM_KERNEL_AUTO):
+        cpt.cpt_set_sum_kernel(k)

@@ -55,11 +55,11 @@ KERNELS = ["auto", "loads", "bulk"]
 @pytest.fixture
 def kernel(cpt, request):
     """Run the test with the requested kernel choice, then restore the default."""
-    code = {"auto": cpt.CPT_GRAD_RETURN_AUTO, "loads": cpt.CPT_GRAD_RETURN_LOADS,
-            "bulk": cpt.CPT_GRAD_RETURN_BULK}[request.param]
-    cpt.cpt_set_grad_return_kernel(code)
+    code = {"auto": cpt.CPT_SUM_KERNEL_AUTO, "loads": cpt.CPT_SUM_KERNEL_LOADS,
+            "bulk": cpt.CPT_SUM_KERNEL_BULK}[request.param]
+    cpt.cpt_set_sum_kernel(code)
     yield request.param
-    cpt.cpt_set_grad_return_kernel(cpt.CPT_GRAD_RETURN_AUTO)
+    cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO)
 
 
 def _ids(c):

@@ -3,8 +3,10 @@ call of the C ABI, each output compared with the oracle bit for bit.
 
 Each case draws a layout, P in 1..8, a document mix (zero-length documents
 included), a row width that is a multiple of 16 bytes but not of a warp's
-512 bytes, and a dtype pair. The fixed cases elsewhere pin known corners;
-this sweep looks for the corners nobody thought of.
+512 bytes, and a dtype pair, and runs once under the measured kernel rule
+and once with the bulk-copy gradient return forced. The fixed cases
+elsewhere pin known corners; this sweep looks for the corners nobody
+thought of.
 """
 import numpy as np
 import pytest
@@ -47,8 +49,20 @@ def _tdt(dt):
     return torch.float32 if dt == "f32" else torch.bfloat16
 
 
+@pytest.fixture(params=["auto", "bulk"])
+def sum_kernel(cpt, request):
+    """Each case runs under the measured kernel rule, and again with the
+    bulk-copy gradient return forced wherever it can run (equal types,
+    overwrite mode), so that kernel also meets rows of any width from 16
+    bytes up."""
+    cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO if request.param == "auto"
+                                   else cpt.CPT_SUM_KERNEL_BULK)
+    yield request.param
+    cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO)
+
+
 @pytest.mark.parametrize("seed", range(40))
-def test_random_case_every_call(cpt, cuda_device, seed):
+def test_random_case_every_call(cpt, cuda_device, seed, sum_kernel):
     rng, layout, P, lens, row, din, dout = _case(seed)
     cu = synth.cu_from_lengths(lens)
     T = int(cu[-1])
@@ -114,3 +128,8 @@ def test_random_case_every_call(cpt, cuda_device, seed):
         assert np.array_equal(bits(got[o]), bits(want[o])), (seed, o)
         assert np.array_equal(bits(got_acc[o]), bits(want_acc[o])), (seed, o)
         assert np.array_equal(bits(got_pieces[o]), bits(want[o])), (seed, o)
+
+
+def test_random_sweep_no_bulk_wait_ran_out(cpt, cuda_device):
+    torch.cuda.synchronize()
+    assert cpt.cpt_kernel_wait_timeouts() == 0
