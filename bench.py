@@ -85,12 +85,38 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _device_code(text: str) -> str:
+    """The parts of a .cu file that decide what its kernels do: every
+    `constexpr` line and every `__global__` function (from its template line
+    through its closing brace). Host launch code is left out, so an edit
+    there does not invalidate a traffic record."""
+    import re
+
+    parts = [line for line in text.splitlines() if line.lstrip().startswith("constexpr ")]
+    for m in re.finditer(r"(?m)^(template <[^\n]*>\n)?__global__", text):
+        start = m.start()
+        i = text.index("{", m.end())
+        depth = 0
+        for j in range(i, len(text)):
+            if text[j] == "{":
+                depth += 1
+            elif text[j] == "}":
+                depth -= 1
+                if depth == 0:
+                    parts.append(text[start:j + 1])
+                    break
+    return "\n".join(parts)
+
+
 def kernel_source_hash() -> str:
+    """Hash of the gradient-return kernels' device code (all of
+    cpt_device.cuh, the kernels and constants of grad_return.cu)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "context_attention_token_gb300", "csrc")
-    for name in ("grad_return.cu", "cpt_device.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+    with open(os.path.join(csrc, "cpt_device.cuh")) as f:
+        h.update(f.read().encode())
+    with open(os.path.join(csrc, "grad_return.cu")) as f:
+        h.update(_device_code(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -12,6 +12,8 @@
 // at a time and moves it in 16-byte units, kUnroll units per lane in flight
 // before the first store. Rows are visited in output order by a grid-stride
 // loop, so concurrently active warps read and write neighbouring rows.
+#include <atomic>
+
 #include "cpt_device.cuh"
 #include "cpt_internal.h"
 
@@ -63,18 +65,18 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p)
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream)
 {
     if (p.rows == 0) return cudaSuccess;
-    static int blocks_per_sm[64] = {0};  // per device
+    static std::atomic<int> blocks_per_sm[64];  // per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (blocks_per_sm[dev] == 0) {
+    if (blocks_per_sm[dev].load(std::memory_order_acquire) == 0) {
         int per_sm = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel, kThreads, 0);
         if (e != cudaSuccess) return e;
-        blocks_per_sm[dev] = per_sm > 0 ? per_sm : 1;
+        blocks_per_sm[dev].store(per_sm > 0 ? per_sm : 1, std::memory_order_release);
     }
-    const int64_t cap = (int64_t)blocks_per_sm[dev] * sm_count(dev);
+    const int64_t cap = (int64_t)blocks_per_sm[dev].load(std::memory_order_acquire) * sm_count(dev);
     int64_t blocks = (p.rows + (kThreads / 32) - 1) / (kThreads / 32);  // one warp per row
     if (blocks > cap) blocks = cap;
     gather_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p);

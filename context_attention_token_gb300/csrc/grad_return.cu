@@ -286,28 +286,31 @@ template <int P, int T>
 cudaError_t launch_bulk(const GradReturnParams &p, size_t smem, cudaStream_t stream)
 {
     auto kernel = grad_return_bulk_kernel<P, T>;
-    // per device: whether the shared-memory limit is raised, and the
-    // occupancy of the last shared-memory size asked for
-    static bool attr_set[64] = {false};
-    static size_t cached_smem[64] = {0};
-    static int cached_per_sm[64] = {0};
+    // Per device: whether the shared-memory limit is raised, and the
+    // occupancy of the last shared-memory size asked for, packed into one
+    // word as (smem << 8) | CTAs per SM so that concurrent callers never pair
+    // one size with another's occupancy.
+    static std::atomic<bool> attr_set[64];
+    static std::atomic<int64_t> occupancy[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkMaxSmem);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
-    if (cached_smem[dev] != smem) {
+    int64_t packed = occupancy[dev].load(std::memory_order_relaxed);
+    if ((packed >> 8) != (int64_t)smem) {
         int per_sm = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32 * kBulkWarps, smem);
         if (e != cudaSuccess) return e;
-        cached_per_sm[dev] = per_sm > 0 ? per_sm : 1;
-        cached_smem[dev] = smem;
+        per_sm = per_sm < 1 ? 1 : (per_sm > 255 ? 255 : per_sm);
+        packed = ((int64_t)smem << 8) | per_sm;
+        occupancy[dev].store(packed, std::memory_order_relaxed);
     }
-    int64_t blocks = (int64_t)cached_per_sm[dev] * sm_count(dev);
+    int64_t blocks = (packed & 0xFF) * (int64_t)sm_count(dev);
     const int64_t needed = (p.rows + kBulkWarps - 1) / kBulkWarps;
     if (blocks > needed) blocks = needed;
     kernel<<<(unsigned)blocks, 32 * kBulkWarps, smem, stream>>>(p);
@@ -326,18 +329,18 @@ cudaError_t launch_typed(const GradReturnParams &p, cudaStream_t stream)
     }
     constexpr int U = P <= 4 ? 2 : 1;
     auto kernel = grad_return_kernel<P, IN, OUT, U, ACC>;
-    static int blocks_per_sm[64] = {0};  // per device, one table per instantiation
+    static std::atomic<int> blocks_per_sm[64];  // per device, one table per instantiation
     int dev = 0;
     const cudaError_t dev_err = cudaGetDevice(&dev);
     if (dev_err != cudaSuccess) return dev_err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (blocks_per_sm[dev] == 0) {
+    if (blocks_per_sm[dev].load(std::memory_order_acquire) == 0) {
         int n = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0);
         if (e != cudaSuccess) return e;
-        blocks_per_sm[dev] = n > 0 ? n : 1;
+        blocks_per_sm[dev].store(n > 0 ? n : 1, std::memory_order_release);
     }
-    const int64_t cap = (int64_t)blocks_per_sm[dev] * sm_count(dev);
+    const int64_t cap = (int64_t)blocks_per_sm[dev].load(std::memory_order_acquire) * sm_count(dev);
     int64_t blocks = (p.rows + (kThreads / 32) - 1) / (kThreads / 32);
     if (blocks > cap) blocks = cap;
     kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p);

@@ -19,6 +19,8 @@
 //    mbarrier, sums them there, and writes the chunk back with one bulk store.
 //    Whole chunks only; the rest goes to slot_reduce_kernel. Every mbarrier
 //    wait has a budget; one that runs out is counted in g_wait_timeouts.
+#include <atomic>
+
 #include "cpt_device.cuh"
 #include "cpt_internal.h"
 
@@ -206,20 +208,20 @@ cudaError_t launch_bulk(const SlotReduceParams &p, int64_t n_chunks, cudaStream_
 {
     auto kernel = slot_reduce_bulk_kernel<P, T>;
     constexpr size_t smem = (size_t)kBulkWarps * (P + 1) * kChunk;
-    static int blocks_per_sm[64] = {0};
+    static std::atomic<int> blocks_per_sm[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (blocks_per_sm[dev] == 0) {
+    if (blocks_per_sm[dev].load(std::memory_order_acquire) == 0) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         int n = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 32 * kBulkWarps, smem);
         if (e != cudaSuccess) return e;
-        blocks_per_sm[dev] = n > 0 ? n : 1;
+        blocks_per_sm[dev].store(n > 0 ? n : 1, std::memory_order_release);
     }
-    int64_t blocks = (int64_t)blocks_per_sm[dev] * sm_count(dev);
+    int64_t blocks = (int64_t)blocks_per_sm[dev].load(std::memory_order_acquire) * sm_count(dev);
     const int64_t needed = (n_chunks + kBulkWarps - 1) / kBulkWarps;
     if (blocks > needed) blocks = needed;
     kernel<<<(unsigned)blocks, 32 * kBulkWarps, smem, stream>>>(p, n_chunks);
@@ -272,18 +274,18 @@ cudaError_t launch_loads(const SlotReduceParams &p, cudaStream_t stream)
     constexpr int U = P <= 4 ? 2 : 1;
     constexpr int E = IN == kBf16 ? 8 : 4;
     auto kernel = slot_reduce_kernel<P, IN, OUT, U>;
-    static int blocks_per_sm[64] = {0};
+    static std::atomic<int> blocks_per_sm[64];
     int dev = 0;
     const cudaError_t dev_err = cudaGetDevice(&dev);
     if (dev_err != cudaSuccess) return dev_err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (blocks_per_sm[dev] == 0) {
+    if (blocks_per_sm[dev].load(std::memory_order_acquire) == 0) {
         int n = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0);
         if (e != cudaSuccess) return e;
-        blocks_per_sm[dev] = n > 0 ? n : 1;
+        blocks_per_sm[dev].store(n > 0 ? n : 1, std::memory_order_release);
     }
-    const int64_t cap = (int64_t)blocks_per_sm[dev] * sm_count(dev);
+    const int64_t cap = (int64_t)blocks_per_sm[dev].load(std::memory_order_acquire) * sm_count(dev);
     const int64_t n_units = p.n_elems / E;
     int64_t blocks = (n_units + (int64_t)kThreads * U - 1) / ((int64_t)kThreads * U);
     if (blocks < 1) blocks = 1;
