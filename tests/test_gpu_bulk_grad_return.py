@@ -147,6 +147,52 @@ def test_bulk_grad_return_noalloc(cpt, cuda_device, case, kernel):
             assert np.array_equal(got[o], want[o]), f"owner {o}"
 
 
+def test_bulk_kernel_from_concurrent_host_threads(cpt, cuda_device):
+    """Four host threads, each on its own stream, launch the bulk kernel over
+    and over with different row sizes, so the launcher's per-size occupancy
+    cache keeps changing under them. Every result equals the oracle's."""
+    import threading
+
+    cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_BULK)
+    try:
+        jobs = []
+        for k, row in enumerate((512, 1024, 2560, 640)):
+            layout, P, cu, T, Tpad, l2g, wk, wv, code = _setup((DSC, 4, [8, 56, 200], row, "bf16"), 7400 + k)
+            plan = cpt.cpt_plan_create(layout, P, cu, T)
+            dkw = torch.stack([to_dev(w) for w in wk])
+            dvw = torch.stack([to_dev(w) for w in wv])
+            outs = [(torch.empty((P, Tpad // P, row), dtype=torch.bfloat16, device="cuda"),
+                     torch.empty((P, Tpad // P, row), dtype=torch.bfloat16, device="cuda")) for _ in range(3)]
+            want = (oracle.grad_return(l2g, wk, code), oracle.grad_return(l2g, wv, code))
+            jobs.append((plan, dkw, dvw, outs, want, torch.cuda.Stream()))
+        torch.cuda.synchronize()
+        errors = []
+
+        def run(job):
+            plan, dkw, dvw, outs, _, stream = job
+            try:
+                for it in range(30):
+                    ko, vo = outs[it % 3]
+                    cpt.cpt_grad_return(plan, dkw, dvw, ko, vo, stream=stream)
+            except Exception as e:  # reported on the main thread
+                errors.append(e)
+
+        threads = [threading.Thread(target=run, args=(j,)) for j in jobs]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+        torch.cuda.synchronize()
+        assert not errors, errors
+        for plan, dkw, dvw, outs, want, _ in jobs:
+            for ko, vo in outs:
+                got_k, got_v = to_host(ko), to_host(vo)
+                for o in range(4):
+                    assert np.array_equal(got_k[o], want[0][o]) and np.array_equal(got_v[o], want[1][o])
+    finally:
+        cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO)
+
+
 def test_no_bulk_copy_wait_ran_out(cpt, cuda_device):
     """Every bulk-copy wait above completed within its budget."""
     torch.cuda.synchronize()
