@@ -9,15 +9,15 @@
 //
 // HBM-bound: per output row it reads P input rows and writes one. Two kernels
 // share the arithmetic (binary32 adds in writer order):
-//  - grad_return_bulk_kernel, for equal input and output types, overwrite,
-//    and the cp_size, row and launch sizes where it measured faster
-//    (prefer_bulk; set_sum_kernel overrides): every warp runs its own
-//    row pipeline.
-//    Lane 0 brings the P writer rows into shared memory with P bulk copies
-//    (cp.async.bulk) counted on one mbarrier, the warp sums them out of
-//    shared memory into a staged output row, and lane 0 writes that row back
-//    with one bulk store. Every mbarrier wait has a time and poll budget; a
-//    wait that runs out is counted in g_wait_timeouts and stops the warp.
+//  - grad_return_bulk_kernel, for equal input and output types, overwrite
+//    mode, and the cp_size, row and launch sizes where it measured faster
+//    (prefer_bulk; set_sum_kernel overrides the rule). Every warp runs its
+//    own row pipeline: lane 0 brings the P writer rows into shared memory
+//    with P bulk copies (cp.async.bulk) counted on one mbarrier, the warp
+//    sums them out of shared memory into a staged output row, and lane 0
+//    writes that row back with one bulk store. Every mbarrier wait has a
+//    time and poll budget; a wait that runs out is counted in
+//    g_wait_timeouts and stops the warp.
 //  - grad_return_kernel, for all other cases (mixed types, accumulate mode,
 //    short rows): a warp owns one output row at a time and each lane keeps
 //    U x P 16-byte loads in flight before summing.
@@ -43,10 +43,10 @@ constexpr int kBulkMaxSmem = 112 * 1024;      // keeps two CTAs (four warps) on 
 // about 20 % wherever its shared memory leaves one CTA per SM.
 //
 // With L2 flushed before every launch (as after an attention backward that
-// has just written the writer rows), the bulk kernel also starts more slowly:
-// at P = 4 and 6 it lost 1-7 % on launches of 0.17 to 1.3 GB and won from
-// about 2.7 GB (P = 4: even at 2.7 GB, -1 to -2 % at 5.4 GB; P = 6: -1.5 %
-// at 2.7 GB, -4.5 % at 5.4 GB), while at P = 8 it won at almost every size.
+// has just written the writer rows), the bulk kernel also starts more
+// slowly. At P = 4 and 6 it lost 1-7 % on launches of 0.17 to 1.3 GB. At
+// 2.7 GB it tied at P = 4 and won by 1.5 % at P = 6; at 5.4 GB it won by
+// 1-2 % at P = 4 and 4.5 % at P = 6. At P = 8 it won at almost every size.
 // So for P <= 6 the rule also asks for launches of at least 2 GiB.
 constexpr int64_t kBulkMinLaunchBytes = int64_t(2) << 30;
 
