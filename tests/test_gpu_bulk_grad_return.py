@@ -109,8 +109,11 @@ ROW_RANGE_CASES = [c for c in CASES if c[3] * (4 if c[4] == "f32" else 2) >= 409
 @pytest.mark.parametrize("kernel", KERNELS, indirect=True)
 @pytest.mark.parametrize("case", ROW_RANGE_CASES, ids=_ids)
 def test_bulk_grad_return_dk_only_and_row_ranges(cpt, cuda_device, case, kernel):
-    """dK alone (no dV pair), then the same sums as three row ranges."""
-    layout, P, cu, T, Tpad, l2g, wk, _wv, code = _setup(case, 7200 + case[1])
+    """dK alone (no dV pair), then the same sums as three row ranges, then
+    dK and dV together over three other row ranges (the launch's row index
+    crosses from the dK half to the dV half, and the range offset applies to
+    both)."""
+    layout, P, cu, T, Tpad, l2g, wk, wv, code = _setup(case, 7200 + case[1])
     odt = torch.float32 if case[4] == "f32" else torch.bfloat16
     row = case[3]
     plan = cpt.cpt_plan_create(layout, P, cu, T)
@@ -122,11 +125,22 @@ def test_bulk_grad_return_dk_only_and_row_ranges(cpt, cuda_device, case, kernel)
     for a, b in zip(cuts, cuts[1:]):
         cpt.cpt_grad_return_rows(plan, dkw, None, pieces, None, a, b - a)
     torch.cuda.synchronize()
+    dvw = torch.stack([to_dev(w) for w in wv])
+    pk = torch.full((P, Tpad // P, row), 3.0, dtype=odt, device="cuda")
+    pv = torch.full((P, Tpad // P, row), 5.0, dtype=odt, device="cuda")
+    cuts2 = [0, 1, Tpad // 2, Tpad]
+    for a, b in zip(cuts2, cuts2[1:]):
+        cpt.cpt_grad_return_rows(plan, dkw, dvw, pk, pv, a, b - a)
+    torch.cuda.synchronize()
     want = oracle.grad_return(l2g, wk, code)
+    want_v = oracle.grad_return(l2g, wv, code)
     got_w, got_p = to_host(whole), to_host(pieces)
+    got_k2, got_v2 = to_host(pk), to_host(pv)
     for o in range(P):
         assert np.array_equal(bits(got_w[o]), bits(want[o])), f"owner {o}"
         assert np.array_equal(bits(got_p[o]), bits(want[o])), f"owner {o}"
+        assert np.array_equal(bits(got_k2[o]), bits(want[o])), f"owner {o}"
+        assert np.array_equal(bits(got_v2[o]), bits(want_v[o])), f"owner {o}"
 
 
 @pytest.mark.parametrize("kernel", ["loads", "bulk"], indirect=True)
