@@ -453,8 +453,8 @@ def run_gpu(args):
         dist.barrier()
     from context_attention_token_gb300 import cpt, synth
 
-    cpt.cpt_set_sum_kernel({"auto": cpt.CPT_SUM_KERNEL_AUTO, "loads": cpt.CPT_SUM_KERNEL_LOADS,
-                                    "bulk": cpt.CPT_SUM_KERNEL_BULK}[args.sum_kernel])
+    cpt.cpt_set_kernel_path({"auto": cpt.CPT_KERNEL_AUTO, "loads": cpt.CPT_KERNEL_LOADS,
+                                    "bulk": cpt.CPT_KERNEL_BULK}[args.kernel_path])
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
 
@@ -675,7 +675,7 @@ def run_gpu(args):
         "data": "synthetic (seeded device N(0,1) Q/K/V, N(0,0.02) dK/dV)",
         "config": {"workload": workload(), "P": P, "S": S, "H": H, "D": D,
                    "layout": "dual_chunk_swap", "grad_return_path": PATH,
-                   "sum_kernel": args.sum_kernel,
+                   "kernel_path": args.kernel_path,
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (21.5 GB touched per step), no flush",
                    "step_bytes": step_bytes(S)},
@@ -842,12 +842,12 @@ def run_next_rows(args):
                 lambda: cpt.cpt_grad_return_noalloc(0, Pw, [0, S], S, dkw, dvw, dko, dvo), stream)
             emit("grad_return_noalloc_P4", ms, S * (2 * (Pw + 1) * row + 2 * 4) + S * 4, P=Pw, S=S,
                  note="includes its own map build (index-map kernel) each call")
-            for kname, kcode in (("loads", cpt.CPT_SUM_KERNEL_LOADS), ("bulk", cpt.CPT_SUM_KERNEL_BULK)):
-                cpt.cpt_set_sum_kernel(kcode)
+            for kname, kcode in (("loads", cpt.CPT_KERNEL_LOADS), ("bulk", cpt.CPT_KERNEL_BULK)):
+                cpt.cpt_set_kernel_path(kcode)
                 ms = _median_launch_ms(lambda: cpt.cpt_grad_return(planp, dkw, dvw, dko, dvo), stream)
                 emit(f"grad_return_P4_{kname}_kernel", ms, S * (2 * (Pw + 1) * row + 2 * 4), P=Pw, S=S,
                      kernel=kname)
-            cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO)
+            cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
         del dkw, dvw, dko, dvo
         torch.cuda.empty_cache()
 
@@ -867,9 +867,9 @@ def run_next_rows(args):
         wv = synth.device_normal_bf16((P, Tg, Hg, D), 6401, 1.0, "cuda")
         ok = torch.empty((P, Tg // P, Hg, D), dtype=torch.bfloat16, device="cuda")
         ov = torch.empty_like(ok)
-        for kname, kcode in (("", cpt.CPT_SUM_KERNEL_AUTO), ("_loads_kernel", cpt.CPT_SUM_KERNEL_LOADS),
-                             ("_bulk_kernel", cpt.CPT_SUM_KERNEL_BULK)):
-            cpt.cpt_set_sum_kernel(kcode)
+        for kname, kcode in (("", cpt.CPT_KERNEL_AUTO), ("_loads_kernel", cpt.CPT_KERNEL_LOADS),
+                             ("_bulk_kernel", cpt.CPT_KERNEL_BULK)):
+            cpt.cpt_set_kernel_path(kcode)
             evs = []
             for it in range(23):
                 flush.zero_()
@@ -883,7 +883,7 @@ def run_next_rows(args):
             ms = statistics.median(x.elapsed_time(y) for x, y in evs)
             emit(name + kname, ms, Tg * (2 * (P + 1) * Hg * D * 2 + 2 * 4), P=P, T=Tg, docs=len(lens_g),
                  l2="flushed before each launch", kernel=kname.strip("_").replace("_kernel", "") or "auto")
-        cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO)
+        cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
         del wk, wv, ok, ov
         torch.cuda.empty_cache()
     del flush
@@ -986,8 +986,8 @@ def run_slot_reduce_sweep(args):
     from context_attention_token_gb300 import cpt
 
     torch.cuda.set_device(0)
-    cpt.cpt_set_sum_kernel({"auto": cpt.CPT_SUM_KERNEL_AUTO, "loads": cpt.CPT_SUM_KERNEL_LOADS,
-                            "bulk": cpt.CPT_SUM_KERNEL_BULK}[args.sum_kernel])
+    cpt.cpt_set_kernel_path({"auto": cpt.CPT_KERNEL_AUTO, "loads": cpt.CPT_KERNEL_LOADS,
+                            "bulk": cpt.CPT_KERNEL_BULK}[args.kernel_path])
     peak, peak_src = load_peak()
     stream = torch.cuda.Stream()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
@@ -1048,7 +1048,7 @@ def run_slot_reduce_sweep(args):
             gbs = (n_slots + 1) * nbytes / (cold_us * 1e-6) / 1e9
             line = {"sweep": "slot_reduce", "metric": "slot_reduce latency and effective GB/s",
                     "dtype": "f32" if dtype == torch.float32 else "bf16", "slots": n_slots,
-                    "sum_kernel": args.sum_kernel,
+                    "kernel_path": args.kernel_path,
                     "bytes_per_slot": nbytes, "iters": iters,
                     "us_per_call_launched": call_us, "us_per_call_graph": graph_us,
                     "us_per_call_cold_l2": cold_us,
@@ -1093,7 +1093,7 @@ def main():
     ap.add_argument("--sweep", choices=["slot_reduce", "host_link"], default=None,
                     help="instead of the step: the slot-reduce message-size sweep, or the "
                          "host link's copy rates")
-    ap.add_argument("--sum-kernel", choices=["auto", "loads", "bulk"], default="auto",
+    ap.add_argument("--kernel-path", choices=["auto", "loads", "bulk"], default="auto",
                     help="kernel of the gradient return and the slot reduce: the measured rule "
                          "(default), or one forced")
     ap.add_argument("--slots", type=int, default=8, help="--sweep slot_reduce: number of slots (1..8)")

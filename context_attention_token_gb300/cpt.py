@@ -51,9 +51,9 @@ CPT_BF16 = 1
 CPT_WAIT_BOUNDED = 0
 CPT_WAIT_DRIVER = 1
 CPT_MAX_CP_SIZE = 8
-CPT_SUM_KERNEL_AUTO = 0
-CPT_SUM_KERNEL_LOADS = 1
-CPT_SUM_KERNEL_BULK = 2
+CPT_KERNEL_AUTO = 0
+CPT_KERNEL_LOADS = 1
+CPT_KERNEL_BULK = 2
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -100,7 +100,7 @@ _sig("cpt_epoch_publish", ctypes.c_int, _vp, _i32, _vp)
 _sig("cpt_epoch_wait", ctypes.c_int, _vp, _i32, _u64, ctypes.c_int, _vp)
 _sig("cpt_epoch_status", ctypes.c_int, _vp, _i32, _vp, ctypes.POINTER(_i32))
 _sig("cpt_kernel_wait_timeouts", ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), _i32)
-_sig("cpt_set_sum_kernel", ctypes.c_int, _i32)
+_sig("cpt_set_kernel_path", ctypes.c_int, _i32)
 _sig("cpt_slot_reduce", ctypes.c_int, _vp, _i32, _i64, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp)
 
 
@@ -485,10 +485,10 @@ def cpt_epoch_status(ep: Epoch, owner: int, stream=None) -> int:
     return v.value
 
 
-def cpt_set_sum_kernel(kernel: int):
+def cpt_set_kernel_path(kernel: int):
     """Process-wide kernel choice of the fused gradient return:
-    CPT_SUM_KERNEL_AUTO (measured rule), _LOADS or _BULK."""
-    _check(_lib.cpt_set_sum_kernel(kernel))
+    CPT_KERNEL_AUTO (measured rule), _LOADS or _BULK."""
+    _check(_lib.cpt_set_kernel_path(kernel))
 
 
 def cpt_kernel_wait_timeouts(reset: bool = False) -> int:

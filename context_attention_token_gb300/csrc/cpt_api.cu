@@ -997,12 +997,12 @@ cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *stream, in
     return CPT_OK;
 }
 
-cpt_status cpt_set_sum_kernel(cpt_sum_kernel kernel)
+cpt_status cpt_set_kernel_path(cpt_kernel_path kernel)
 {
-    Trace trace("cpt_set_sum_kernel");
-    if (kernel != CPT_SUM_KERNEL_AUTO && kernel != CPT_SUM_KERNEL_LOADS && kernel != CPT_SUM_KERNEL_BULK)
+    Trace trace("cpt_set_kernel_path");
+    if (kernel != CPT_KERNEL_AUTO && kernel != CPT_KERNEL_LOADS && kernel != CPT_KERNEL_BULK)
         return fail(CPT_ERR_INVALID_ARG, "unknown gradient return kernel %d", (int)kernel);
-    set_sum_kernel((int)kernel);
+    set_kernel_path((int)kernel);
     return CPT_OK;
 }
 
@@ -1012,11 +1012,12 @@ cpt_status cpt_kernel_wait_timeouts(uint32_t *count, int32_t reset)
     if (count == nullptr) return fail(CPT_ERR_INVALID_ARG, "NULL argument");
     int dev = 0;
     if (!current_device(&dev)) return fail(CPT_ERR_DEVICE, "no current CUDA device");
-    unsigned int v = 0, w = 0;
+    unsigned int v = 0, w = 0, x = 0;
     cudaError_t e = read_wait_timeouts(&v, reset != 0);
     if (e == cudaSuccess) e = read_slot_reduce_wait_timeouts(&w, reset != 0);
+    if (e == cudaSuccess) e = read_gather_wait_timeouts(&x, reset != 0);
     if (e != cudaSuccess) return cuda_fail(e, "wait-timeout counter read");
-    *count = v + w;
+    *count = v + w + x;
     return CPT_OK;
 }
 

@@ -68,17 +68,18 @@ struct GradReturnParams {
     int32_t in_row_bytes;
     int32_t out_row_bytes;
 };
-// Kernel of the fused gradient return and the slot reduce: 0 = the measured
-// rule, 1 = 16-byte loads, 2 = bulk copies wherever they can run.
-// Process-wide.
-void set_sum_kernel(int choice);
-int sum_kernel();
+// Kernel of the row gather, the fused gradient return and the slot reduce:
+// 0 = the measured rule, 1 = 16-byte loads, 2 = bulk copies wherever they can
+// run. Process-wide.
+void set_kernel_path(int choice);
+int kernel_path();
 
 // Reads (and, if reset, zeroes) the count of bulk-copy waits in the gradient
 // return kernel that ran out of their budget, on the current device.
 // Synchronous.
 cudaError_t read_wait_timeouts(unsigned int *count, bool reset);
 cudaError_t read_slot_reduce_wait_timeouts(unsigned int *count, bool reset);
+cudaError_t read_gather_wait_timeouts(unsigned int *count, bool reset);
 
 cudaError_t launch_grad_return(const GradReturnParams &p, int cp_size, int in_dtype,
                                int out_dtype, cudaStream_t stream, bool accumulate = false);

@@ -8,10 +8,21 @@
 //    index = l2g, one destination pointer per owner;
 //  - the padded layout: index -1 marks a padding row, written as zeros.
 //
-// HBM-bound bit copy: every output row is one source row. A warp owns one row
-// at a time and moves it in 16-byte units, kUnroll units per lane in flight
-// before the first store. Rows are visited in output order by a grid-stride
-// loop, so concurrently active warps read and write neighbouring rows.
+// HBM-bound bit copy: every output row is one source row. Two kernels:
+//  - gather_blocks_kernel (long rows and large launches, where it measured
+//    faster: prefer_blocks; set_kernel_path overrides): the output is cut
+//    into blocks of up to kBlockBytes of consecutive rows. One thread per CTA
+//    moves each block through shared memory with bulk copies
+//    (cp.async.bulk): source rows with consecutive indices share one bulk
+//    load, destination rows of one rank piece share one bulk store, padding
+//    rows are zero-filled in shared memory. A ring of kStages blocks keeps
+//    loads in flight while earlier blocks are stored; the warp reads the map
+//    one block ahead. Every mbarrier wait has a time and poll budget; a wait
+//    that runs out is counted in g_wait_timeouts and stops the CTA.
+//  - gather_kernel (all other cases): a warp owns one row at a time and
+//    moves it in 16-byte units, kUnroll units per lane in flight before the
+//    first store. Rows are visited in output order by a grid-stride loop, so
+//    concurrently active warps read and write neighbouring rows.
 #include <atomic>
 
 #include "cpt_device.cuh"
@@ -23,6 +34,20 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
+
+// The blocks kernel's shape, from a sweep on GB300 (blocks of 10 to 60 KB, 2
+// to 6 stages, 1 to 3 CTAs per SM; rows of 2, 4 and 5 KB, P = 4 and 8; L2
+// flushed before every launch): about 40 KB per block, four stages and one
+// CTA per SM was fastest or within 1 % of it at every row size, and 4 to 7 %
+// faster than gather_kernel.
+constexpr int kStages = 4;
+constexpr int kBlockBytes = 40960;
+constexpr int kMaxBlockRows = 32;  // one map entry per lane
+constexpr int kBlocksMaxSmem = 200 * 1024;
+
+// Bulk-copy waits that ran out of their budget; zero unless a copy never
+// completed. Read by read_gather_wait_timeouts.
+__device__ unsigned int g_wait_timeouts;
 
 __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p)
 {
@@ -60,7 +85,183 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p)
     }
 }
 
+
+// Block b of tensor t covers the launch's local rows [q0 + b*B, +n), n <= B.
+// Block indices and rows stay below 2^31 (T < 2^31), so 32-bit division does.
+__global__ void __launch_bounds__(32) gather_blocks_kernel(const GatherParams p, const int B)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bar[kStages];
+    const int lane = threadIdx.x;
+    const int64_t rb = p.row_bytes;
+    const uint32_t per_t = (uint32_t)((p.T + B - 1) / B);
+    const uint32_t Tp32 = (uint32_t)p.Tp;
+    const int64_t nblk = (int64_t)per_t * (p.rows / p.T);
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t mine = first < nblk ? (nblk - 1 - first) / step + 1 : 0;
+    uint32_t phases = 0;  // bit s: parity of the phase stage s waits for next
+
+    struct Blk {
+        uint32_t t;
+        int64_t L0;
+        int n;
+    };
+    auto block = [&](int64_t i) {
+        const uint32_t blk = (uint32_t)(first + i * step);
+        Blk b;
+        b.t = blk / per_t;
+        b.L0 = (int64_t)(blk - b.t * per_t) * B;
+        b.n = (int)min((int64_t)B, p.T - b.L0);
+        return b;
+    };
+    // this lane's map entry for the i-th block (-2: no row)
+    auto map_entry = [&](int64_t i) -> int64_t {
+        if (i >= mine) return -2;
+        const Blk b = block(i);
+        if (lane >= b.n) return -2;
+        const int64_t q = p.q0 + b.L0 + lane;
+        return p.l2g ? (int64_t)__ldg(p.l2g + q) : q;
+    };
+    int64_t g_ahead = map_entry(0);
+
+    // whole warp: start the loads of the i-th block into stage i % kStages
+    auto issue = [&](int64_t i) {
+        const Blk b = block(i);
+        const int s = (int)(i % kStages);
+        uint8_t *stage = smem + (size_t)s * B * rb;
+        const int64_t g = g_ahead;
+        g_ahead = map_entry(i + 1);
+        const int64_t g0 = __shfl_sync(0xFFFFFFFFu, g, 0);
+        if (__all_sync(0xFFFFFFFFu, lane >= b.n || (g0 >= 0 && g == g0 + lane))) {
+            if (lane == 0) {  // one contiguous source run
+                mbar_expect_tx(&bar[s], (uint32_t)(b.n * rb));
+                bulk_load(stage, p.src[b.t] + g0 * rb, (uint32_t)(b.n * rb), &bar[s]);
+            }
+            return;
+        }
+        const int real = __popc(__ballot_sync(0xFFFFFFFFu, lane < b.n && g >= 0));
+        if (lane == 0) mbar_expect_tx(&bar[s], (uint32_t)(real * rb));
+        int run0 = 0;
+        int64_t run_g = g0;
+        for (int j = 1; j <= b.n; ++j) {
+            const int64_t gj = __shfl_sync(0xFFFFFFFFu, g, j & 31);
+            const int64_t gp = __shfl_sync(0xFFFFFFFFu, g, j - 1);
+            if (j < b.n && gp >= 0 && gj == gp + 1) continue;  // the run goes on
+            if (lane == 0) {
+                if (run_g >= 0) {
+                    bulk_load(stage + (size_t)run0 * rb, p.src[b.t] + run_g * rb, (uint32_t)((j - run0) * rb),
+                              &bar[s]);
+                } else {  // a padding row (runs of padding are one row long)
+                    for (int64_t u = 0; u < rb; u += 16)
+                        *reinterpret_cast<uint4 *>(stage + (size_t)run0 * rb + u) = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();  // before the bulk store reads it
+                }
+            }
+            run0 = j;
+            run_g = gj;
+        }
+    };
+    // lane 0: store the i-th block, one bulk store per rank piece it touches
+    auto store = [&](int64_t i) {
+        const Blk b = block(i);
+        const uint8_t *stage = smem + (size_t)(i % kStages) * B * rb;
+        int j = 0;
+        while (j < b.n) {
+            const uint32_t q = (uint32_t)(p.q0 + b.L0 + j);
+            const uint32_t r = q / Tp32;
+            const uint32_t jj = q - r * Tp32;
+            const int len = (int)min((int64_t)(b.n - j), (int64_t)(Tp32 - jj));
+            bulk_store(p.dst[b.t][r] + (int64_t)jj * rb, stage + (size_t)j * rb, (uint32_t)(len * rb));
+            j += len;
+        }
+    };
+
+    for (int64_t i = 0; i < kStages - 1 && i < mine; ++i) issue(i);
+    for (int64_t i = 0; i < mine; ++i) {
+        const int s = (int)(i % kStages);
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_bounded(&bar[s], (phases >> s) & 1u);
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+            if (lane == 0) {
+                atomicAdd(&g_wait_timeouts, 1u);
+                // one more budget for every block whose loads may be in flight
+                for (int64_t k = i; k < i + kStages - 1 && k < mine; ++k)
+                    mbar_wait_bounded(&bar[k % kStages], (phases >> (k % kStages)) & 1u);
+            }
+            break;
+        }
+        phases ^= 1u << s;
+        if (lane == 0) store(i);
+        const int64_t nxt = i + kStages - 1;
+        if (nxt < mine) {
+            // the next block reuses the stage of block i - 1, whose stores
+            // are older than block i's: wait until only block i's may read
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+            issue(nxt);
+        }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+}
+
+// The measured rule for the blocks kernel. A sweep on GB300 (partition and
+// restore, rows of 1, 2 and 5 KB, launches of 25 MB to 8 GB, L2 flushed
+// before each launch) found it 4-7 % faster from about 0.5 GB per launch
+// with rows of 2 KB and more, even or slower on smaller launches (up to
+// 13 % slower at 0.2 GB with 2 KB rows), and slower at every size with 1 KB
+// rows. So: rows of at least 2 KB and launches that move at least 384 MiB.
+constexpr int64_t kBlocksMinRowBytes = 2048;
+constexpr int64_t kBlocksMinLaunchBytes = int64_t(384) << 20;
+
+bool prefer_blocks(const GatherParams &p)
+{
+    return p.row_bytes >= kBlocksMinRowBytes && 2 * p.rows * p.row_bytes >= kBlocksMinLaunchBytes;
+}
+
+// Rows per block for rows of row_bytes, or 0 when the blocks kernel cannot
+// take them (its stages would not fit in shared memory).
+int block_rows(int64_t row_bytes)
+{
+    int64_t B = kBlockBytes / row_bytes;
+    B = B < 1 ? 1 : (B > kMaxBlockRows ? kMaxBlockRows : B);
+    return (int64_t)kStages * B * row_bytes <= kBlocksMaxSmem ? (int)B : 0;
+}
+
+cudaError_t launch_blocks(const GatherParams &p, int B, int dev, cudaStream_t stream)
+{
+    static std::atomic<bool> attr_set[64];
+    cudaError_t e;
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(gather_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kBlocksMaxSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev].store(true, std::memory_order_release);
+    }
+    const size_t smem = (size_t)kStages * B * p.row_bytes;
+    const int64_t nblk = (p.T + B - 1) / B * (p.rows / p.T);
+    int64_t grid = sm_count(dev);  // one CTA per SM
+    if (grid > nblk) grid = nblk;
+    gather_blocks_kernel<<<(unsigned)grid, 32, smem, stream>>>(p, B);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t read_gather_wait_timeouts(unsigned int *count, bool reset)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(unsigned int));
+    if (e == cudaSuccess && reset) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
 
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream)
 {
@@ -70,6 +271,9 @@ cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const int choice = kernel_path();
+    const int B = block_rows(p.row_bytes);
+    if (B > 0 && (choice == 2 || (choice == 0 && prefer_blocks(p)))) return launch_blocks(p, B, dev, stream);
     if (blocks_per_sm[dev].load(std::memory_order_acquire) == 0) {
         int per_sm = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel, kThreads, 0);

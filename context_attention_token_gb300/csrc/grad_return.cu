@@ -11,7 +11,7 @@
 // share the arithmetic (binary32 adds in writer order):
 //  - grad_return_bulk_kernel, for equal input and output types, overwrite
 //    mode, and the cp_size, row and launch sizes where it measured faster
-//    (prefer_bulk; set_sum_kernel overrides the rule). Every warp runs its
+//    (prefer_bulk; set_kernel_path overrides the rule). Every warp runs its
 //    own row pipeline: lane 0 brings the P writer rows into shared memory
 //    with P bulk copies (cp.async.bulk) counted on one mbarrier, the warp
 //    sums them out of shared memory into a staged output row, and lane 0
@@ -66,7 +66,7 @@ bool prefer_bulk(int P, int type, int64_t row_bytes, int64_t launch_bytes)
 }
 
 // 0 = the measured rule, 1 = always the 16-byte-load kernel, 2 = the bulk
-// kernel wherever it can run (set_sum_kernel).
+// kernel wherever it can run (set_kernel_path).
 std::atomic<int> g_kernel_choice{0};
 
 // Bulk-copy waits that ran out of their budget (see mbar_wait_bounded); zero
@@ -374,12 +374,12 @@ cudaError_t launch_acc(const GradReturnParams &p, int cp_size, int in, int out, 
 
 }  // namespace
 
-void set_sum_kernel(int choice)
+void set_kernel_path(int choice)
 {
     g_kernel_choice.store(choice, std::memory_order_relaxed);
 }
 
-int sum_kernel()
+int kernel_path()
 {
     return g_kernel_choice.load(std::memory_order_relaxed);
 }

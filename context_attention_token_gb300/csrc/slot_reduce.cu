@@ -252,7 +252,7 @@ cudaError_t launch_typed(const SlotReduceParams &p, cudaStream_t stream)
     if constexpr (IN == OUT) {
         constexpr int esz = IN == kBf16 ? 2 : 4;
         const int64_t bytes = p.n_elems * esz;
-        if (use_bulk(sum_kernel(), P, bytes)) {
+        if (use_bulk(kernel_path(), P, bytes)) {
             const int64_t n_chunks = bytes / kChunk;
             cudaError_t e = launch_bulk<P, IN>(p, n_chunks, stream);
             if (e != cudaSuccess) return e;

@@ -135,13 +135,13 @@ typedef enum cpt_dtype { CPT_F32 = 0, CPT_BF16 = 1 } cpt_dtype;
  *           writer's publish of this epoch is already enqueued. */
 typedef enum cpt_wait_mode { CPT_WAIT_BOUNDED = 0, CPT_WAIT_DRIVER = 1 } cpt_wait_mode;
 
-/* Which kernel the ordered sums run: the fused gradient return and the slot
- * reduce (cpt_set_sum_kernel). */
-typedef enum cpt_sum_kernel {
-    CPT_SUM_KERNEL_AUTO = 0,  /* the measured rule (default) */
-    CPT_SUM_KERNEL_LOADS = 1, /* 16-byte loads into registers */
-    CPT_SUM_KERNEL_BULK = 2   /* bulk copies through shared memory, where it can run */
-} cpt_sum_kernel;
+/* Which kernel the HBM-bound calls run: the row gather, the fused gradient
+ * return and the slot reduce (cpt_set_kernel_path). */
+typedef enum cpt_kernel_path {
+    CPT_KERNEL_AUTO = 0,  /* the measured rule (default) */
+    CPT_KERNEL_LOADS = 1, /* 16-byte loads into registers */
+    CPT_KERNEL_BULK = 2   /* bulk copies through shared memory, where it can run */
+} cpt_kernel_path;
 
 typedef struct cpt_plan cpt_plan;   /* opaque: layout, P, T, pointers into the workspace */
 typedef struct cpt_epoch cpt_epoch; /* opaque: epoch counter and publish bookkeeping    */
@@ -371,24 +371,29 @@ CPT_API cpt_status cpt_grad_return_accumulate(const cpt_plan *plan, const void *
                                               int64_t row_elems, cpt_dtype in, cpt_dtype out,
                                               void *stream);
 
-/* Choose the kernel of the two ordered sums, for the whole process and every
+/* Choose the kernel of the HBM-bound calls, for the whole process and every
  * device (paper has no counterpart: a tuning and testing control of this
- * implementation). The choice covers the fused gradient return
- * (cpt_grad_return, cpt_grad_return_rows, cpt_grad_return_noalloc) and
- * cpt_slot_reduce. Both kernels compute the same bits.
- *  - CPT_SUM_KERNEL_LOADS: each lane keeps P 16-byte loads in flight in
- *    registers. Every case can run it.
- *  - CPT_SUM_KERNEL_BULK: each warp stages P rows (gradient return: one
- *    owner row's writer rows; slot reduce: 4 KB of every slot) in shared
- *    memory with bulk copies and stores the sum with one bulk copy. It needs
- *    equal input and output types. For the gradient return it also needs
- *    overwrite mode (not cpt_grad_return_accumulate) and 2 x (P+1) x row
- *    bytes of at most 112 KB. Where these do not hold, the loads kernel
- *    runs; the slot reduce also sums its last partial 4 KB with it.
- *  - CPT_SUM_KERNEL_AUTO (the default): bulk where it measured faster on
- *    GB300, loads elsewhere.
- *    Gradient return: rows of at least 1 KB, and for P <= 6 launches of
- *    at least 2 GiB, with these row sizes per P:
+ * implementation). The choice covers the row gather (cpt_partition,
+ * cpt_partition_rows, cpt_restore, cpt_grad_scatter), the fused gradient
+ * return (cpt_grad_return, cpt_grad_return_rows, cpt_grad_return_noalloc)
+ * and cpt_slot_reduce. Both kernels of each call compute the same bits.
+ *  - CPT_KERNEL_LOADS: each lane keeps 16-byte loads in flight in registers.
+ *    Every case can run it.
+ *  - CPT_KERNEL_BULK: data moves through shared memory with bulk copies.
+ *    Row gather: blocks of up to 40 KB of consecutive rows, one bulk load
+ *    per contiguous source run and one bulk store per rank piece; it needs
+ *    4 blocks to fit in 200 KB. Gradient return: one owner row's P writer
+ *    rows per warp; it needs equal input and output types, overwrite mode
+ *    (not cpt_grad_return_accumulate) and 2 x (P+1) x row bytes of at most
+ *    112 KB. Slot reduce: 4 KB of every slot per warp; it needs equal input
+ *    and output types, and sums its last partial 4 KB with the loads
+ *    kernel. Where a condition fails, the loads kernel runs.
+ *  - CPT_KERNEL_AUTO (the default): bulk where it measured faster on GB300,
+ *    loads elsewhere.
+ *    Row gather: rows of at least 2 KB in launches that move at least
+ *    384 MiB.
+ *    Gradient return: rows of at least 1 KB, and for P <= 6 launches of at
+ *    least 2 GiB, with these row sizes per P:
  *      P >= 5: any row size;
  *      P = 4:  bf16 rows of at least 2 KB, float32 rows of at most 2 KB;
  *      P = 3:  bf16 rows of at least 3 KB;
@@ -397,7 +402,7 @@ CPT_API cpt_status cpt_grad_return_accumulate(const cpt_plan *plan, const void *
  *  The choice applies to calls made after this one returns. Concurrent
  *  calls from other threads see either the old or the new choice.
  *  Errors: CPT_ERR_INVALID_ARG (not one of the three values). */
-CPT_API cpt_status cpt_set_sum_kernel(cpt_sum_kernel kernel);
+CPT_API cpt_status cpt_set_kernel_path(cpt_kernel_path kernel);
 
 /* Largest batch cpt_grad_return_noalloc accepts. */
 #define CPT_NOALLOC_MAX_TOKENS 1048576
@@ -518,9 +523,9 @@ CPT_API cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *st
 /* Count of bounded waits inside this library's kernels that ran out of
  * their budget on the current device, since the library was loaded or last
  * reset (paper has no counterpart: it is this implementation's failure
- * report). The bulk-copy kernels of the gradient return and the slot
- * reduce move data through shared memory, each copy completing on an
- * mbarrier. Every wait on one gives up after about a second or 2^24 polls.
+ * report). The bulk-copy kernels of the row gather, the gradient return and
+ * the slot reduce move data through shared memory, each copy completing on
+ * an mbarrier. Every wait on one gives up after about a second or 2^24 polls.
  * A wait that gives up is counted here, its warp stops, and the outputs it
  * had not reached are left unwritten. A non-zero count means some output
  * of an earlier call is not valid.

@@ -155,10 +155,10 @@ def test_binding_constants_match_header(cpt):
         assert getattr(cpt, name) == val, name
 
 
-def test_sum_kernel_choice_validated(cpt):
+def test_kernel_path_choice_validated(cpt):
     """The kernel choice takes the three enumerators and refuses anything else."""
     for bad in (-1, 3, 99):
         with pytest.raises(cpt.CptError):
-            cpt.cpt_set_sum_kernel(bad)
-    for k in (cpt.CPT_SUM_KERNEL_LOADS, cpt.CPT_SUM_KERNEL_BULK, cpt.CPT_SUM_KERNEL_AUTO):
-        cpt.cpt_set_sum_kernel(k)
+            cpt.cpt_set_kernel_path(bad)
+    for k in (cpt.CPT_KERNEL_LOADS, cpt.CPT_KERNEL_BULK, cpt.CPT_KERNEL_AUTO):
+        cpt.cpt_set_kernel_path(k)

@@ -55,11 +55,11 @@ KERNELS = ["auto", "loads", "bulk"]
 @pytest.fixture
 def kernel(cpt, request):
     """Run the test with the requested kernel choice, then restore the default."""
-    code = {"auto": cpt.CPT_SUM_KERNEL_AUTO, "loads": cpt.CPT_SUM_KERNEL_LOADS,
-            "bulk": cpt.CPT_SUM_KERNEL_BULK}[request.param]
-    cpt.cpt_set_sum_kernel(code)
+    code = {"auto": cpt.CPT_KERNEL_AUTO, "loads": cpt.CPT_KERNEL_LOADS,
+            "bulk": cpt.CPT_KERNEL_BULK}[request.param]
+    cpt.cpt_set_kernel_path(code)
     yield request.param
-    cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO)
+    cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
 
 
 def _ids(c):
@@ -167,7 +167,7 @@ def test_bulk_kernel_from_concurrent_host_threads(cpt, cuda_device):
     cache keeps changing under them. Every result equals the oracle's."""
     import threading
 
-    cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_BULK)
+    cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_BULK)
     try:
         jobs = []
         for k, row in enumerate((512, 1024, 2560, 640)):
@@ -204,7 +204,7 @@ def test_bulk_kernel_from_concurrent_host_threads(cpt, cuda_device):
                 for o in range(4):
                     assert np.array_equal(got_k[o], want[0][o]) and np.array_equal(got_v[o], want[1][o])
     finally:
-        cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO)
+        cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
 
 
 def test_no_bulk_copy_wait_ran_out(cpt, cuda_device):

@@ -22,11 +22,11 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(params=["auto", "loads", "bulk"])
 def kernel(cpt, request):
-    code = {"auto": cpt.CPT_SUM_KERNEL_AUTO, "loads": cpt.CPT_SUM_KERNEL_LOADS,
-            "bulk": cpt.CPT_SUM_KERNEL_BULK}[request.param]
-    cpt.cpt_set_sum_kernel(code)
+    code = {"auto": cpt.CPT_KERNEL_AUTO, "loads": cpt.CPT_KERNEL_LOADS,
+            "bulk": cpt.CPT_KERNEL_BULK}[request.param]
+    cpt.cpt_set_kernel_path(code)
     yield request.param
-    cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO)
+    cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
 
 
 def _elems(nbytes, dt):

@@ -50,19 +50,19 @@ def _tdt(dt):
 
 
 @pytest.fixture(params=["auto", "bulk"])
-def sum_kernel(cpt, request):
+def kernel_path(cpt, request):
     """Each case runs under the measured kernel rule, and again with the
     bulk-copy gradient return forced wherever it can run (equal types,
     overwrite mode), so that kernel also meets rows of any width from 16
     bytes up."""
-    cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO if request.param == "auto"
-                                   else cpt.CPT_SUM_KERNEL_BULK)
+    cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO if request.param == "auto"
+                                   else cpt.CPT_KERNEL_BULK)
     yield request.param
-    cpt.cpt_set_sum_kernel(cpt.CPT_SUM_KERNEL_AUTO)
+    cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
 
 
 @pytest.mark.parametrize("seed", range(40))
-def test_random_case_every_call(cpt, cuda_device, seed, sum_kernel):
+def test_random_case_every_call(cpt, cuda_device, seed, kernel_path):
     rng, layout, P, lens, row, din, dout = _case(seed)
     cu = synth.cu_from_lengths(lens)
     T = int(cu[-1])
