@@ -816,8 +816,20 @@ def run_next_rows(args):
         cpt.cpt_plan_destroy(pl)
         del graph, ws_l, l2g_l, g2l_l, meta
 
-    # f1: restore K and V from rank-local back to global order
+    # the Q/K/V partition at the pages' shape under each gather kernel
     plan = cpt.cpt_plan_create(0, P, [0, S], S)
+    qkv_p = [synth.device_normal_bf16((S, H, D), 5900 + t, 1.0, "cuda") for t in range(3)]
+    out_p = [torch.empty((P, S // P, H, D), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    for kname, kcode in (("", cpt.CPT_KERNEL_AUTO), ("_loads_kernel", cpt.CPT_KERNEL_LOADS),
+                         ("_bulk_kernel", cpt.CPT_KERNEL_BULK)):
+        cpt.cpt_set_kernel_path(kcode)
+        ms = _median_launch_ms(lambda: cpt.cpt_partition(plan, qkv_p, out_p), stream)
+        emit("partition_pages_shape" + kname, ms, S * (3 * 2 * row + 3 * 4), S=S, P=P,
+             tok_s=S / (ms / 1e3), kernel=kname.strip("_").replace("_kernel", "") or "auto")
+    cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
+    del qkv_p, out_p
+
+    # f1: restore K and V from rank-local back to global order
     kv = [synth.device_normal_bf16((P, S // P, H, D), 6000 + t, 1.0, "cuda") for t in range(2)]
     back = [torch.empty((S, H, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     ms = _median_launch_ms(lambda: cpt.cpt_restore(plan, kv, back), stream)
