@@ -101,6 +101,7 @@ _sig("cpt_epoch_wait", ctypes.c_int, _vp, _i32, _u64, ctypes.c_int, _vp)
 _sig("cpt_epoch_status", ctypes.c_int, _vp, _i32, _vp, ctypes.POINTER(_i32))
 _sig("cpt_kernel_wait_timeouts", ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), _i32)
 _sig("cpt_set_kernel_path", ctypes.c_int, _i32)
+_sig("cpt_test_stall_bulk_waits", ctypes.c_int, _i32)
 _sig("cpt_slot_reduce", ctypes.c_int, _vp, _i32, _i64, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp)
 
 
@@ -489,6 +490,12 @@ def cpt_set_kernel_path(kernel: int):
     """Process-wide kernel choice of the fused gradient return:
     CPT_KERNEL_AUTO (measured rule), _LOADS or _BULK."""
     _check(_lib.cpt_set_kernel_path(kernel))
+
+
+def cpt_test_stall_bulk_waits(on: bool):
+    """Test switch: make every bulk-copy wait of later launches run out of its
+    budget (on) or behave normally (off)."""
+    _check(_lib.cpt_test_stall_bulk_waits(1 if on else 0))
 
 
 def cpt_kernel_wait_timeouts(reset: bool = False) -> int:

@@ -1006,6 +1006,19 @@ cpt_status cpt_set_kernel_path(cpt_kernel_path kernel)
     return CPT_OK;
 }
 
+cpt_status cpt_test_stall_bulk_waits(int32_t on)
+{
+    Trace trace("cpt_test_stall_bulk_waits");
+    int dev = 0;
+    if (!current_device(&dev)) return fail(CPT_ERR_DEVICE, "no current CUDA device");
+    const unsigned int extra = on ? 16u : 0u;
+    cudaError_t e = set_stall_grad_return(extra);
+    if (e == cudaSuccess) e = set_stall_slot_reduce(extra);
+    if (e == cudaSuccess) e = set_stall_gather(extra);
+    if (e != cudaSuccess) return cuda_fail(e, "stall switch");
+    return CPT_OK;
+}
+
 cpt_status cpt_kernel_wait_timeouts(uint32_t *count, int32_t reset)
 {
     Trace trace("cpt_kernel_wait_timeouts");

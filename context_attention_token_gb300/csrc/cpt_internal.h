@@ -81,6 +81,13 @@ cudaError_t read_wait_timeouts(unsigned int *count, bool reset);
 cudaError_t read_slot_reduce_wait_timeouts(unsigned int *count, bool reset);
 cudaError_t read_gather_wait_timeouts(unsigned int *count, bool reset);
 
+// Test hook: every bulk-copy mbarrier of later launches on the current device
+// announces extra_bytes more than its copies deliver, so its waits run out
+// (0 = normal). Synchronous.
+cudaError_t set_stall_grad_return(unsigned int extra_bytes);
+cudaError_t set_stall_slot_reduce(unsigned int extra_bytes);
+cudaError_t set_stall_gather(unsigned int extra_bytes);
+
 cudaError_t launch_grad_return(const GradReturnParams &p, int cp_size, int in_dtype,
                                int out_dtype, cudaStream_t stream, bool accumulate = false);
 

@@ -49,6 +49,11 @@ constexpr int kBlocksMaxSmem = 200 * 1024;
 // completed. Read by read_gather_wait_timeouts.
 __device__ unsigned int g_wait_timeouts;
 
+// Extra bytes announced on every bulk-copy mbarrier beyond what its copies
+// deliver: 0, except while a test makes the waits run out on purpose
+// (set_stall_gather).
+__device__ unsigned int g_stall_tx;
+
 __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p)
 {
     const int lane = threadIdx.x & 31;
@@ -105,6 +110,7 @@ __global__ void __launch_bounds__(32) gather_blocks_kernel(const GatherParams p,
     const int64_t first = blockIdx.x, step = gridDim.x;
     const int64_t mine = first < nblk ? (nblk - 1 - first) / step + 1 : 0;
     uint32_t phases = 0;  // bit s: parity of the phase stage s waits for next
+    const uint32_t stall = g_stall_tx;
 
     struct Blk {
         uint32_t t;
@@ -139,13 +145,13 @@ __global__ void __launch_bounds__(32) gather_blocks_kernel(const GatherParams p,
         const int64_t g0 = __shfl_sync(0xFFFFFFFFu, g, 0);
         if (__all_sync(0xFFFFFFFFu, lane >= b.n || (g0 >= 0 && g == g0 + lane))) {
             if (lane == 0) {  // one contiguous source run
-                mbar_expect_tx(&bar[s], (uint32_t)(b.n * rb));
+                mbar_expect_tx(&bar[s], (uint32_t)(b.n * rb) + stall);
                 bulk_load(stage, p.src[b.t] + g0 * rb, (uint32_t)(b.n * rb), &bar[s]);
             }
             return;
         }
         const int real = __popc(__ballot_sync(0xFFFFFFFFu, lane < b.n && g >= 0));
-        if (lane == 0) mbar_expect_tx(&bar[s], (uint32_t)(real * rb));
+        if (lane == 0) mbar_expect_tx(&bar[s], (uint32_t)(real * rb) + stall);
         int run0 = 0;
         int64_t run_g = g0;
         for (int j = 1; j <= b.n; ++j) {
@@ -252,6 +258,11 @@ cudaError_t launch_blocks(const GatherParams &p, int B, int dev, cudaStream_t st
 }
 
 }  // namespace
+
+cudaError_t set_stall_gather(unsigned int extra_bytes)
+{
+    return cudaMemcpyToSymbol(g_stall_tx, &extra_bytes, sizeof(unsigned int));
+}
 
 cudaError_t read_gather_wait_timeouts(unsigned int *count, bool reset)
 {

@@ -73,6 +73,11 @@ std::atomic<int> g_kernel_choice{0};
 // unless a copy never completed. Read and reset by read_wait_timeouts.
 __device__ unsigned int g_wait_timeouts;
 
+// Extra bytes announced on every bulk-copy mbarrier beyond what its copies
+// deliver: 0, except while a test makes the waits run out on purpose
+// (set_stall_grad_return).
+__device__ unsigned int g_stall_tx;
+
 // Elements of one 16-byte input unit, widened to binary32.
 template <int IN>
 struct Unit;
@@ -225,6 +230,7 @@ __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const
     const int64_t stride = (int64_t)gridDim.x * kBulkWarps;
     int64_t R = (int64_t)blockIdx.x * kBulkWarps + wid;
     int64_t g_next = 0;
+    const uint32_t stall = g_stall_tx;
     if (lane == 0 && R < p.rows) g_next = __ldg(p.l2g + p.q0 + (R >= p.T ? R - p.T : R));
     uint32_t phase = 0;
 
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const
         const int64_t j = q - (int64_t)o * p.Tp;
         if (lane == 0) {
             const int64_t g = g_next;
-            mbar_expect_tx(bar, (uint32_t)(P * rb));
+            mbar_expect_tx(bar, (uint32_t)(P * rb) + stall);
 #pragma unroll
             for (int w = 0; w < P; ++w)
                 bulk_load(stage + (size_t)w * rb, (t ? p.w[1][w] : p.w[0][w]) + g * rb, (uint32_t)rb,
@@ -382,6 +388,11 @@ void set_kernel_path(int choice)
 int kernel_path()
 {
     return g_kernel_choice.load(std::memory_order_relaxed);
+}
+
+cudaError_t set_stall_grad_return(unsigned int extra_bytes)
+{
+    return cudaMemcpyToSymbol(g_stall_tx, &extra_bytes, sizeof(unsigned int));
 }
 
 cudaError_t read_wait_timeouts(unsigned int *count, bool reset)

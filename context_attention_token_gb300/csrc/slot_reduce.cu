@@ -37,6 +37,11 @@ constexpr int kBulkMaxSmem = 112 * 1024;
 // completed. Read by read_slot_reduce_wait_timeouts.
 __device__ unsigned int g_wait_timeouts;
 
+// Extra bytes announced on every bulk-copy mbarrier beyond what its copies
+// deliver: 0, except while a test makes the waits run out on purpose
+// (set_stall_slot_reduce).
+__device__ unsigned int g_stall_tx;
+
 template <int IN>
 __device__ __forceinline__ float load_scalar(const uint8_t *base, int64_t i)
 {
@@ -156,10 +161,11 @@ __global__ void __launch_bounds__(32 * kBulkWarps) slot_reduce_bulk_kernel(const
     }
     __syncwarp();
     uint32_t phase = 0;
+    const uint32_t stall = g_stall_tx;
     const int64_t stride = (int64_t)gridDim.x * kBulkWarps;
     for (int64_t c = (int64_t)blockIdx.x * kBulkWarps + wid; c < n_chunks; c += stride) {
         if (lane == 0) {
-            mbar_expect_tx(bar, (uint32_t)(P * kChunk));
+            mbar_expect_tx(bar, (uint32_t)(P * kChunk) + stall);
 #pragma unroll
             for (int w = 0; w < P; ++w) bulk_load(stage + (size_t)w * kChunk, p.s[w] + c * kChunk, kChunk, bar);
         }
@@ -336,6 +342,11 @@ __global__ void epoch_check_kernel(const uint32_t *flags_row, int P, uint32_t ep
 }
 
 }  // namespace
+
+cudaError_t set_stall_slot_reduce(unsigned int extra_bytes)
+{
+    return cudaMemcpyToSymbol(g_stall_tx, &extra_bytes, sizeof(unsigned int));
+}
 
 cudaError_t read_slot_reduce_wait_timeouts(unsigned int *count, bool reset)
 {

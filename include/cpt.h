@@ -536,6 +536,18 @@ CPT_API cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *st
  *  Errors: CPT_ERR_INVALID_ARG (NULL count), CPT_ERR_DEVICE, CPT_ERR_CUDA. */
 CPT_API cpt_status cpt_kernel_wait_timeouts(uint32_t *count, int32_t reset);
 
+/* Test switch for the failure path of the bulk-copy kernels (paper has no
+ * counterpart). While on, every bulk-copy mbarrier of later launches on the
+ * current device announces 16 bytes more than its copies deliver. Every
+ * copy still completes, and nothing faults, but each wait runs out of its
+ * budget (about a second). The kernels count the timeouts
+ * (cpt_kernel_wait_timeouts) and stop early, leaving outputs unwritten; a
+ * stalled launch takes a few seconds. Off (0) by default; turn it off
+ * again before relying on any output.
+ *  Blocking: writes device memory synchronously.
+ *  Errors: CPT_ERR_DEVICE, CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_test_stall_bulk_waits(int32_t on);
+
 /* ------------------------------------------------------------------ */
 /* Ordered slot reduce                                                 */
 /* ------------------------------------------------------------------ */
