@@ -61,7 +61,7 @@ def kernel_path(cpt, request):
     cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
 
 
-@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("seed", range(100))
 def test_random_case_every_call(cpt, cuda_device, seed, kernel_path):
     rng, layout, P, lens, row, din, dout = _case(seed)
     cu = synth.cu_from_lengths(lens)
