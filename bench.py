@@ -596,61 +596,95 @@ def run_gpu(args):
             pieces += [(g0 + a, q0 + a, b - a) for a, b in zip(cut, cut[1:]) if b > a]
         h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
 
-        def e2e_step():
-            # Three streams, one per resource: host-to-device copies of every
-            # piece back to back on h2d_stream, the kernels of a piece on the
-            # main stream once its rows are in, its rows out on d2h_stream once
-            # its kernels are done. A step starts after the previous one ended
-            # on every stream, so no buffer is overwritten while still in use.
-            h2d_stream.wait_stream(stream)
-            d2h_stream.wait_stream(stream)
+        # Two device buffer sets, used by alternate steps, so that a step's
+        # copies in can run while the previous step's results are still being
+        # copied out: the host link carries both directions at once, and its
+        # host-to-device side never waits for a step boundary.
+        sets = [(qkv, dkw, dvw, part, dko, dvo),
+                ([torch.empty_like(x) for x in qkv], torch.empty_like(dkw), torch.empty_like(dvw),
+                 [torch.empty_like(x) for x in part], torch.empty_like(dko), torch.empty_like(dvo))]
+        kernels_done = [None, None]   # per set: the last kernel of the step that used it
+        outputs_out = [None, None]    # per set: the last copy out of the step that used it
+
+        def e2e_step(i):
+            # Three streams, one per resource: copies in of every piece back to
+            # back on h2d_stream, the kernels of a piece on the main stream once
+            # its rows are in, its rows out on d2h_stream once its kernels are
+            # done. A set's inputs are overwritten only after the kernels that
+            # read them (two steps back) are done, and its outputs only after
+            # they were copied out.
+            s_qkv, s_dkw, s_dvw, s_part, s_dko, s_dvo = sets[i % 2]
             plan = cpt.cpt_plan_create(cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP, P, cu, S, workspace=ws)
+            if kernels_done[i % 2] is not None:
+                h2d_stream.wait_event(kernels_done[i % 2])
+            if outputs_out[i % 2] is not None:
+                stream.wait_event(outputs_out[i % 2])
             for g0, q0, c in pieces:
                 with torch.cuda.stream(h2d_stream):
-                    for d, h in zip(qkv, h_qkv):
+                    for d, h in zip(s_qkv, h_qkv):
                         d[g0:g0 + c].copy_(h[g0:g0 + c], non_blocking=True)
                     qkv_in = torch.cuda.Event()
                     qkv_in.record(h2d_stream)
                     for w in range(P):
-                        dkw[w, g0:g0 + c].copy_(h_dkw[w, g0:g0 + c], non_blocking=True)
-                        dvw[w, g0:g0 + c].copy_(h_dvw[w, g0:g0 + c], non_blocking=True)
+                        s_dkw[w, g0:g0 + c].copy_(h_dkw[w, g0:g0 + c], non_blocking=True)
+                        s_dvw[w, g0:g0 + c].copy_(h_dvw[w, g0:g0 + c], non_blocking=True)
                     grads_in = torch.cuda.Event()
                     grads_in.record(h2d_stream)
                 stream.wait_event(qkv_in)
-                cpt.cpt_partition_rows(plan, qkv, part, q0, c)
+                cpt.cpt_partition_rows(plan, s_qkv, s_part, q0, c)
                 part_done = torch.cuda.Event()
                 part_done.record(stream)
                 stream.wait_event(grads_in)
-                cpt.cpt_grad_return_rows(plan, dkw, dvw, dko, dvo, q0, c)
+                cpt.cpt_grad_return_rows(plan, s_dkw, s_dvw, s_dko, s_dvo, q0, c)
                 grads_done = torch.cuda.Event()
                 grads_done.record(stream)
                 with torch.cuda.stream(d2h_stream):
                     d2h_stream.wait_event(part_done)
-                    for h, d in zip(h_part, part):
+                    for h, d in zip(h_part, s_part):
                         flat(h)[q0:q0 + c].copy_(flat(d)[q0:q0 + c], non_blocking=True)
                     d2h_stream.wait_event(grads_done)
-                    flat(h_dko)[q0:q0 + c].copy_(flat(dko)[q0:q0 + c], non_blocking=True)
-                    flat(h_dvo)[q0:q0 + c].copy_(flat(dvo)[q0:q0 + c], non_blocking=True)
-            stream.wait_stream(h2d_stream)
-            stream.wait_stream(d2h_stream)
+                    flat(h_dko)[q0:q0 + c].copy_(flat(s_dko)[q0:q0 + c], non_blocking=True)
+                    flat(h_dvo)[q0:q0 + c].copy_(flat(s_dvo)[q0:q0 + c], non_blocking=True)
+            kernels_done[i % 2] = torch.cuda.Event()
+            kernels_done[i % 2].record(stream)
+            outputs_out[i % 2] = torch.cuda.Event()
+            outputs_out[i % 2].record(d2h_stream)
             cpt.cpt_plan_destroy(plan)
 
+        def join():
+            stream.wait_stream(h2d_stream)
+            stream.wait_stream(d2h_stream)
+
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
-        e2e_step()
+        for i in range(2):  # warm-up: one step on each buffer set
+            e2e_step(i)
+        join()
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        h2d_stream.wait_stream(stream)
+        d2h_stream.wait_stream(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        join()
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(a.elapsed_time(b), dev) / e2e_steps
+        # the results that came back equal the device-resident step's, on
+        # sampled rows of every output (both sets computed the same inputs)
+        g = torch.Generator().manual_seed(7)
+        rows_chk = torch.randint(0, S, (4096,), generator=g)
+        for h, d in zip(h_part + [h_dko, h_dvo], part + [dko, dvo]):
+            if not torch.equal(flat(h)[rows_chk], flat(d)[rows_chk.to(dev)].cpu()):
+                raise RuntimeError("e2e results differ from the device-resident step")
+        del sets
         e2e = {"value": whole_job_gbs(step_bytes(S), 1, world, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": e2e_steps,
-               "pipeline": f"copies in, kernels, copies out on 3 streams over {len(pieces)} pieces"}
+               "pipeline": (f"copies in, kernels, copies out on 3 streams over {len(pieces)} pieces, "
+                            "two buffer sets so consecutive steps overlap")}
         del host_in, host_out
 
     if rank != 0:
