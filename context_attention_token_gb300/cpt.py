@@ -54,6 +54,9 @@ CPT_MAX_CP_SIZE = 8
 CPT_KERNEL_AUTO = 0
 CPT_KERNEL_LOADS = 1
 CPT_KERNEL_BULK = 2
+CPT_CALL_ROW_GATHER = 0
+CPT_CALL_GRAD_RETURN = 1
+CPT_CALL_SLOT_REDUCE = 2
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -102,6 +105,7 @@ _sig("cpt_epoch_status", ctypes.c_int, _vp, _i32, _vp, ctypes.POINTER(_i32))
 _sig("cpt_kernel_wait_timeouts", ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), _i32)
 _sig("cpt_set_kernel_path", ctypes.c_int, _i32)
 _sig("cpt_test_stall_bulk_waits", ctypes.c_int, _i32)
+_sig("cpt_kernel_path_of", ctypes.c_int, _i32, _i32, _i32, _i32, _i32, _i64, _i64, ctypes.POINTER(_i32))
 _sig("cpt_slot_reduce", ctypes.c_int, _vp, _i32, _i64, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp)
 
 
@@ -490,6 +494,15 @@ def cpt_set_kernel_path(kernel: int):
     """Process-wide kernel choice of the fused gradient return:
     CPT_KERNEL_AUTO (measured rule), _LOADS or _BULK."""
     _check(_lib.cpt_set_kernel_path(kernel))
+
+
+def cpt_kernel_path_of(call: int, cp_size: int, in_dtype: int, out_dtype: int, accumulate: bool,
+                       row_bytes: int, rows: int) -> int:
+    """CPT_KERNEL_LOADS or CPT_KERNEL_BULK: the kernel the call would run now."""
+    v = _i32()
+    _check(_lib.cpt_kernel_path_of(call, cp_size, in_dtype, out_dtype, 1 if accumulate else 0,
+                                   row_bytes, rows, ctypes.byref(v)))
+    return v.value
 
 
 def cpt_test_stall_bulk_waits(on: bool):

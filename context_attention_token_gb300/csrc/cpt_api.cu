@@ -1006,6 +1006,29 @@ cpt_status cpt_set_kernel_path(cpt_kernel_path kernel)
     return CPT_OK;
 }
 
+cpt_status cpt_kernel_path_of(cpt_call call, int32_t cp_size, cpt_dtype in, cpt_dtype out,
+                              int32_t accumulate, int64_t row_bytes, int64_t rows,
+                              cpt_kernel_path *kernel)
+{
+    if (kernel == nullptr) return fail(CPT_ERR_INVALID_ARG, "NULL argument");
+    if ((in != CPT_F32 && in != CPT_BF16) || (out != CPT_F32 && out != CPT_BF16))
+        return fail(CPT_ERR_INVALID_ARG, "unknown element type");
+    if (row_bytes < 0 || rows < 0) return fail(CPT_ERR_INVALID_ARG, "negative size");
+    if (call != CPT_CALL_ROW_GATHER && (cp_size < 1 || cp_size > CPT_MAX_CP_SIZE))
+        return fail(CPT_ERR_INVALID_ARG, "cp_size %d outside 1..%d", cp_size, CPT_MAX_CP_SIZE);
+    bool bulk;
+    switch (call) {
+    case CPT_CALL_ROW_GATHER: bulk = gather_uses_blocks(row_bytes, rows); break;
+    case CPT_CALL_GRAD_RETURN:
+        bulk = grad_return_uses_bulk(cp_size, (int)in, (int)out, accumulate != 0, row_bytes, rows);
+        break;
+    case CPT_CALL_SLOT_REDUCE: bulk = slot_reduce_uses_bulk(cp_size, (int)in, (int)out, row_bytes); break;
+    default: return fail(CPT_ERR_INVALID_ARG, "unknown call %d", (int)call);
+    }
+    *kernel = bulk ? CPT_KERNEL_BULK : CPT_KERNEL_LOADS;
+    return CPT_OK;
+}
+
 cpt_status cpt_test_stall_bulk_waits(int32_t on)
 {
     Trace trace("cpt_test_stall_bulk_waits");

@@ -74,6 +74,13 @@ struct GradReturnParams {
 void set_kernel_path(int choice);
 int kernel_path();
 
+// The kernel a call runs under the current kernel path (true = the bulk-copy
+// kernel). The launchers decide with these same functions.
+bool gather_uses_blocks(int64_t row_bytes, int64_t rows);
+bool grad_return_uses_bulk(int P, int in_dtype, int out_dtype, bool accumulate, int64_t row_bytes,
+                           int64_t rows);
+bool slot_reduce_uses_bulk(int P, int in_dtype, int out_dtype, int64_t bytes_per_slot);
+
 // Reads (and, if reset, zeroes) the count of bulk-copy waits in the gradient
 // return kernel that ran out of their budget, on the current device.
 // Synchronous.

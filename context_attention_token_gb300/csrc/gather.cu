@@ -225,9 +225,9 @@ __global__ void __launch_bounds__(32) gather_blocks_kernel(const GatherParams p,
 constexpr int64_t kBlocksMinRowBytes = 2048;
 constexpr int64_t kBlocksMinLaunchBytes = int64_t(384) << 20;
 
-bool prefer_blocks(const GatherParams &p)
+bool prefer_blocks(int64_t row_bytes, int64_t rows)
 {
-    return p.row_bytes >= kBlocksMinRowBytes && 2 * p.rows * p.row_bytes >= kBlocksMinLaunchBytes;
+    return row_bytes >= kBlocksMinRowBytes && 2 * rows * row_bytes >= kBlocksMinLaunchBytes;
 }
 
 // Rows per block for rows of row_bytes, or 0 when the blocks kernel cannot
@@ -264,6 +264,13 @@ cudaError_t set_stall_gather(unsigned int extra_bytes)
     return cudaMemcpyToSymbol(g_stall_tx, &extra_bytes, sizeof(unsigned int));
 }
 
+bool gather_uses_blocks(int64_t row_bytes, int64_t rows)
+{
+    if (block_rows(row_bytes) == 0) return false;
+    const int choice = kernel_path();
+    return choice == 2 || (choice == 0 && prefer_blocks(row_bytes, rows));
+}
+
 cudaError_t read_gather_wait_timeouts(unsigned int *count, bool reset)
 {
     cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(unsigned int));
@@ -282,9 +289,7 @@ cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    const int choice = kernel_path();
-    const int B = block_rows(p.row_bytes);
-    if (B > 0 && (choice == 2 || (choice == 0 && prefer_blocks(p)))) return launch_blocks(p, B, dev, stream);
+    if (gather_uses_blocks(p.row_bytes, p.rows)) return launch_blocks(p, block_rows(p.row_bytes), dev, stream);
     if (blocks_per_sm[dev].load(std::memory_order_acquire) == 0) {
         int per_sm = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel, kThreads, 0);

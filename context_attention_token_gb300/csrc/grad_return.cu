@@ -327,11 +327,8 @@ template <int P, int IN, int OUT, bool ACC>
 cudaError_t launch_typed(const GradReturnParams &p, cudaStream_t stream)
 {
     if constexpr (IN == OUT && !ACC) {
-        const int choice = g_kernel_choice.load(std::memory_order_relaxed);
-        const int64_t launch_bytes = p.rows * (P + 1) * (int64_t)p.in_row_bytes;
-        const bool bulk = choice == 2 ? bulk_fits(P, p.in_row_bytes)
-                                      : choice == 0 && prefer_bulk(P, IN, p.in_row_bytes, launch_bytes);
-        if (bulk) return launch_bulk<P, IN>(p, (size_t)kBulkWarps * (P + 1) * p.in_row_bytes, stream);
+        if (grad_return_uses_bulk(P, IN, OUT, false, p.in_row_bytes, p.rows))
+            return launch_bulk<P, IN>(p, (size_t)kBulkWarps * (P + 1) * p.in_row_bytes, stream);
     }
     constexpr int U = P <= 4 ? 2 : 1;
     auto kernel = grad_return_kernel<P, IN, OUT, U, ACC>;
@@ -379,6 +376,15 @@ cudaError_t launch_acc(const GradReturnParams &p, int cp_size, int in, int out, 
 }
 
 }  // namespace
+
+bool grad_return_uses_bulk(int P, int in_dtype, int out_dtype, bool accumulate, int64_t row_bytes,
+                           int64_t rows)
+{
+    if (in_dtype != out_dtype || accumulate) return false;
+    const int choice = g_kernel_choice.load(std::memory_order_relaxed);
+    if (choice == 2) return bulk_fits(P, row_bytes);
+    return choice == 0 && prefer_bulk(P, in_dtype, row_bytes, rows * (P + 1) * row_bytes);
+}
 
 void set_kernel_path(int choice)
 {

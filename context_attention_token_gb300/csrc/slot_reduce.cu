@@ -258,7 +258,7 @@ cudaError_t launch_typed(const SlotReduceParams &p, cudaStream_t stream)
     if constexpr (IN == OUT) {
         constexpr int esz = IN == kBf16 ? 2 : 4;
         const int64_t bytes = p.n_elems * esz;
-        if (use_bulk(kernel_path(), P, bytes)) {
+        if (slot_reduce_uses_bulk(P, IN, OUT, bytes)) {
             const int64_t n_chunks = bytes / kChunk;
             cudaError_t e = launch_bulk<P, IN>(p, n_chunks, stream);
             if (e != cudaSuccess) return e;
@@ -346,6 +346,11 @@ __global__ void epoch_check_kernel(const uint32_t *flags_row, int P, uint32_t ep
 cudaError_t set_stall_slot_reduce(unsigned int extra_bytes)
 {
     return cudaMemcpyToSymbol(g_stall_tx, &extra_bytes, sizeof(unsigned int));
+}
+
+bool slot_reduce_uses_bulk(int P, int in_dtype, int out_dtype, int64_t bytes_per_slot)
+{
+    return in_dtype == out_dtype && use_bulk(kernel_path(), P, bytes_per_slot);
 }
 
 cudaError_t read_slot_reduce_wait_timeouts(unsigned int *count, bool reset)

@@ -404,6 +404,33 @@ CPT_API cpt_status cpt_grad_return_accumulate(const cpt_plan *plan, const void *
  *  Errors: CPT_ERR_INVALID_ARG (not one of the three values). */
 CPT_API cpt_status cpt_set_kernel_path(cpt_kernel_path kernel);
 
+/* The call families cpt_kernel_path_of answers for. */
+typedef enum cpt_call {
+    CPT_CALL_ROW_GATHER = 0,   /* cpt_partition(_rows), cpt_restore, cpt_grad_scatter */
+    CPT_CALL_GRAD_RETURN = 1,  /* cpt_grad_return(_rows, _accumulate, _noalloc) */
+    CPT_CALL_SLOT_REDUCE = 2   /* cpt_slot_reduce */
+} cpt_call;
+
+/* Which kernel a call would run under the current cpt_set_kernel_path
+ * setting, with the same decision the launchers make (paper has no
+ * counterpart). Host-only; touches no device.
+ *  call        the call family.
+ *  cp_size     P: writers for the gradient return, slots for the slot
+ *              reduce (1..8); ignored for the row gather.
+ *  in, out     element types (the gather moves bytes: pass equal types).
+ *  accumulate  non-zero for cpt_grad_return_accumulate.
+ *  row_bytes   bytes of one row (gather, gradient return; the input row for
+ *              the gradient return) or of one slot (slot reduce).
+ *  rows        rows the launch writes: every tensor's rows for the gather;
+ *              all owners' rows of dK (and dV) for the gradient return;
+ *              ignored for the slot reduce.
+ *  kernel      receives CPT_KERNEL_LOADS or CPT_KERNEL_BULK.
+ *  Errors: CPT_ERR_INVALID_ARG (unknown call or type, cp_size outside
+ *  1..8, a negative size, NULL kernel). */
+CPT_API cpt_status cpt_kernel_path_of(cpt_call call, int32_t cp_size, cpt_dtype in, cpt_dtype out,
+                                      int32_t accumulate, int64_t row_bytes, int64_t rows,
+                                      cpt_kernel_path *kernel);
+
 /* Largest batch cpt_grad_return_noalloc accepts. */
 #define CPT_NOALLOC_MAX_TOKENS 1048576
 #define CPT_NOALLOC_MAX_DOCS 65536
