@@ -726,6 +726,14 @@ def run_gpu(args):
                          "how": "torch copy_ of 1 Gi bf16 elements in this run, read+write bytes, "
                                 "best of 10 after 3, CUDA events"},
         "clocks": sampler.summary(t_wall0, t_wall1),
+        "kernels": {
+            "partition": "bulk-copy row blocks" if cpt.cpt_kernel_path_of(
+                cpt.CPT_CALL_ROW_GATHER, P, cpt.CPT_BF16, cpt.CPT_BF16, False, row_bytes(), 3 * S)
+            == cpt.CPT_KERNEL_BULK else "16-byte loads",
+            "grad_return": "bulk-copy row pipelines" if cpt.cpt_kernel_path_of(
+                cpt.CPT_CALL_GRAD_RETURN, P, cpt.CPT_BF16, cpt.CPT_BF16, False, row_bytes(), 2 * S)
+            == cpt.CPT_KERNEL_BULK else "16-byte loads",
+            "path": args.kernel_path},
         "gpu_launches": kernels_per_step * args.steps,
         "e2e": e2e,
     }
