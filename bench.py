@@ -75,6 +75,18 @@ def step_bytes(tokens: int) -> int:
     return tokens * (gr_bytes_per_token() + part_bytes_per_token() + PLAN_BYTES_PER_TOKEN)
 
 
+def host_mem_available():
+    """MemAvailable of this host in bytes, or None where /proc/meminfo is absent."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
 def load_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -558,9 +570,31 @@ def run_gpu(args):
 
     # ---- end to end through the public API with host buffers
     e2e = None
+    e2e_skip = None
     if not args.no_e2e:
-        host_in = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in qkv + [dkw, dvw]]
-        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in part + [dko, dvo]]
+        # every rank on this node pins its own host copy of the step's inputs
+        # and outputs; leave the e2e leg out (with the reason) rather than
+        # exhaust host memory
+        need = sum(x.numel() * x.element_size() for x in qkv + [dkw, dvw] + part + [dko, dvo])
+        local_world = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+        avail = host_mem_available()
+        if avail is not None and need * local_world > 0.8 * avail:
+            e2e_skip = (f"needs {need * local_world / 1e9:.1f} GB of pinned host memory for "
+                        f"{local_world} rank(s), {avail / 1e9:.1f} GB available")
+    if not args.no_e2e and e2e_skip is None:
+        try:
+            host_in = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in qkv + [dkw, dvw]]
+            host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in part + [dko, dvo]]
+        except RuntimeError as err:  # pinned allocation refused
+            e2e_skip = f"pinned host allocation failed: {str(err).splitlines()[0]}"
+    if not args.no_e2e and world > 1:
+        # the e2e leg holds collectives: every rank runs it or none does
+        ok = torch.tensor([0 if e2e_skip else 1], dtype=torch.int32, device=dev)
+        dist.all_reduce(ok, op=dist.ReduceOp.MIN)
+        if int(ok.item()) == 0 and e2e_skip is None:
+            e2e_skip = "another rank could not pin its host buffers"
+            del host_in, host_out
+    if not args.no_e2e and e2e_skip is None:
         for h, d in zip(host_in, qkv + [dkw, dvw]):
             h.copy_(d)
         h2d = sum(x.numel() * x.element_size() for x in host_in)
@@ -735,7 +769,8 @@ def run_gpu(args):
             == cpt.CPT_KERNEL_BULK else "16-byte loads",
             "path": args.kernel_path},
         "gpu_launches": kernels_per_step * args.steps,
-        "e2e": e2e,
+        "e2e": e2e if e2e is not None else ({"value": None, "unit": "GB/s", "skipped": e2e_skip}
+                                            if e2e_skip else None),
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.sample_tokens, args.cpu_budget,
