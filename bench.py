@@ -927,6 +927,13 @@ def run_next_rows(args):
             ms = _median_launch_ms(
                 lambda: cpt.cpt_grad_return_accumulate(planp, dkw, dvw, dko, dvo), stream)
             emit("grad_return_accumulate_P4", ms, S * (2 * (Pw + 2) * row + 2 * 4), P=Pw, S=S)
+            for kname, kcode in (("loads", cpt.CPT_KERNEL_LOADS), ("bulk", cpt.CPT_KERNEL_BULK)):
+                cpt.cpt_set_kernel_path(kcode)
+                ms = _median_launch_ms(
+                    lambda: cpt.cpt_grad_return_accumulate(planp, dkw, dvw, dko, dvo), stream)
+                emit(f"grad_return_accumulate_P4_{kname}_kernel", ms, S * (2 * (Pw + 2) * row + 2 * 4),
+                     P=Pw, S=S, kernel=kname)
+            cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
             ms = _median_launch_ms(
                 lambda: cpt.cpt_grad_return_noalloc(0, Pw, [0, S], S, dkw, dvw, dko, dvo), stream)
             emit("grad_return_noalloc_P4", ms, S * (2 * (Pw + 1) * row + 2 * 4) + S * 4, P=Pw, S=S,

@@ -9,17 +9,17 @@
 //
 // HBM-bound: per output row it reads P input rows and writes one. Two kernels
 // share the arithmetic (binary32 adds in writer order):
-//  - grad_return_bulk_kernel, for equal input and output types, overwrite
-//    mode, and the cp_size, row and launch sizes where it measured faster
-//    (prefer_bulk; set_kernel_path overrides the rule). Every warp runs its
+//  - grad_return_bulk_kernel, for equal input and output types, in the
+//    cp_size, row and launch sizes where it measured faster (prefer_bulk;
+//    set_kernel_path overrides the rule), in either mode. Every warp runs its
 //    own row pipeline: lane 0 brings the P writer rows into shared memory
 //    with P bulk copies (cp.async.bulk) counted on one mbarrier, the warp
 //    sums them out of shared memory into a staged output row, and lane 0
 //    writes that row back with one bulk store. Every mbarrier wait has a
 //    time and poll budget; a wait that runs out is counted in
 //    g_wait_timeouts and stops the warp.
-//  - grad_return_kernel, for all other cases (mixed types, accumulate mode,
-//    short rows): a warp owns one output row at a time and each lane keeps
+//  - grad_return_kernel, for all other cases (mixed types, short rows, small
+//    launches): a warp owns one output row at a time and each lane keeps
 //    U x P 16-byte loads in flight before summing.
 // Both size the grid to whole CTAs per SM and stride over rows in output order.
 #include <atomic>
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kThreads) grad_return_kernel(const GradReturnP
 // Same-type overwrite case through shared memory. Per warp: a stage of P
 // input rows and one output row. Lane 0 issues the loads of a row while the
 // map entry of the row after it is already being fetched.
-template <int P, int T>
+template <int P, int T, bool ACC>
 __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const GradReturnParams p)
 {
     constexpr int E = Unit<T>::kElems;
@@ -241,11 +241,16 @@ __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const
         const int64_t j = q - (int64_t)o * p.Tp;
         if (lane == 0) {
             const int64_t g = g_next;
-            mbar_expect_tx(bar, (uint32_t)(P * rb) + stall);
+            // accumulate mode reloads `out` with the owner's current row: the
+            // previous row's store must have read it first
+            if constexpr (ACC) bulk_wait_read<0>();
+            mbar_expect_tx(bar, (uint32_t)((P + (ACC ? 1 : 0)) * rb) + stall);
 #pragma unroll
             for (int w = 0; w < P; ++w)
                 bulk_load(stage + (size_t)w * rb, (t ? p.w[1][w] : p.w[0][w]) + g * rb, (uint32_t)rb,
                           bar);
+            if constexpr (ACC)
+                bulk_load(out, (t ? p.o[1][o] : p.o[0][o]) + j * p.out_row_bytes, (uint32_t)rb, bar);
             const int64_t Rn = R + stride;
             if (Rn < p.rows) g_next = __ldg(p.l2g + p.q0 + (Rn >= p.T ? Rn - p.T : Rn));
         }
@@ -258,13 +263,14 @@ __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const
             break;
         }
         phase ^= 1u;
-        if (lane == 0) bulk_wait_read<0>();  // the previous row's store has read `out`
+        if (!ACC && lane == 0) bulk_wait_read<0>();  // the previous row's store has read `out`
         __syncwarp();
         for (int u = lane; u < p.units; u += 32) {
             float acc[E];
-            Unit<T>::widen(*reinterpret_cast<const uint4 *>(stage + (size_t)u * 16), acc);
+            // overwrite: start from writer 0; accumulate: from the owner's value
+            Unit<T>::widen(*reinterpret_cast<const uint4 *>((ACC ? out : stage) + (size_t)u * 16), acc);
 #pragma unroll
-            for (int w = 1; w < P; ++w) {
+            for (int w = ACC ? 0 : 1; w < P; ++w) {
                 float x[E];
                 Unit<T>::widen(*reinterpret_cast<const uint4 *>(stage + (size_t)w * rb + (size_t)u * 16), x);
 #pragma unroll
@@ -288,10 +294,10 @@ __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const
     __syncwarp();
 }
 
-template <int P, int T>
+template <int P, int T, bool ACC>
 cudaError_t launch_bulk(const GradReturnParams &p, size_t smem, cudaStream_t stream)
 {
-    auto kernel = grad_return_bulk_kernel<P, T>;
+    auto kernel = grad_return_bulk_kernel<P, T, ACC>;
     // Per device: whether the shared-memory limit is raised, and the
     // occupancy of the last shared-memory size asked for, packed into one
     // word as (smem << 8) | CTAs per SM so that concurrent callers never pair
@@ -326,9 +332,9 @@ cudaError_t launch_bulk(const GradReturnParams &p, size_t smem, cudaStream_t str
 template <int P, int IN, int OUT, bool ACC>
 cudaError_t launch_typed(const GradReturnParams &p, cudaStream_t stream)
 {
-    if constexpr (IN == OUT && !ACC) {
-        if (grad_return_uses_bulk(P, IN, OUT, false, p.in_row_bytes, p.rows))
-            return launch_bulk<P, IN>(p, (size_t)kBulkWarps * (P + 1) * p.in_row_bytes, stream);
+    if constexpr (IN == OUT) {
+        if (grad_return_uses_bulk(P, IN, OUT, ACC, p.in_row_bytes, p.rows))
+            return launch_bulk<P, IN, ACC>(p, (size_t)kBulkWarps * (P + 1) * p.in_row_bytes, stream);
     }
     constexpr int U = P <= 4 ? 2 : 1;
     auto kernel = grad_return_kernel<P, IN, OUT, U, ACC>;
@@ -380,10 +386,16 @@ cudaError_t launch_acc(const GradReturnParams &p, int cp_size, int in, int out, 
 bool grad_return_uses_bulk(int P, int in_dtype, int out_dtype, bool accumulate, int64_t row_bytes,
                            int64_t rows)
 {
-    if (in_dtype != out_dtype || accumulate) return false;
+    if (in_dtype != out_dtype) return false;
     const int choice = g_kernel_choice.load(std::memory_order_relaxed);
     if (choice == 2) return bulk_fits(P, row_bytes);
-    return choice == 0 && prefer_bulk(P, in_dtype, row_bytes, rows * (P + 1) * row_bytes);
+    // the same rule serves both modes; accumulate also reads the owner row.
+    // Measured in accumulate mode on GB300 (L2 flushed / warm): -4.5 % / 0 %
+    // at P=4 with 5 KB rows (16 GB), -7 % / -1 % at P=8, -5 % / -1 % at P=4
+    // with 2 KB rows (6.7 GB), and +4 % at P=4 with 2 KB rows in a 0.8 GB
+    // launch, which the launch-size condition sends to the loads kernel.
+    const int64_t launch_bytes = rows * (P + (accumulate ? 2 : 1)) * row_bytes;
+    return choice == 0 && prefer_bulk(P, in_dtype, row_bytes, launch_bytes);
 }
 
 void set_kernel_path(int choice)

@@ -143,6 +143,31 @@ def test_bulk_grad_return_dk_only_and_row_ranges(cpt, cuda_device, case, kernel)
         assert np.array_equal(bits(got_v2[o]), bits(want_v[o])), f"owner {o}"
 
 
+@pytest.mark.parametrize("kernel", KERNELS, indirect=True)
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_bulk_grad_return_accumulate(cpt, cuda_device, case, kernel):
+    """Accumulate mode: the owners' current rows start the ordered sums (the
+    bulk kernel loads them into its output stage with the writer rows)."""
+    layout, P, cu, T, Tpad, l2g, wk, wv, code = _setup(case, 7500 + case[1])
+    row, dt = case[3], case[4]
+    odt = torch.float32 if dt == "f32" else torch.bfloat16
+    rng = np.random.default_rng(7600 + P)
+    gen = synth.uniform_f32 if dt == "f32" else synth.uniform_bf16
+    starts_k = [gen(rng, (Tpad // P, row)) for _ in range(P)]
+    starts_v = [gen(rng, (Tpad // P, row)) for _ in range(P)]
+    plan = cpt.cpt_plan_create(layout, P, cu, T)
+    ok = torch.stack([to_dev(x) for x in starts_k])
+    ov = torch.stack([to_dev(x) for x in starts_v])
+    cpt.cpt_grad_return_accumulate(plan, torch.stack([to_dev(w) for w in wk]),
+                                   torch.stack([to_dev(w) for w in wv]), ok, ov)
+    torch.cuda.synchronize()
+    for ws, st, out in ((wk, starts_k, ok), (wv, starts_v, ov)):
+        want = oracle.grad_return_accumulate(l2g, ws, st)
+        got = to_host(out)
+        for o in range(P):
+            assert np.array_equal(bits(got[o]), bits(want[o])), f"owner {o}"
+
+
 @pytest.mark.parametrize("kernel", ["loads", "bulk"], indirect=True)
 @pytest.mark.parametrize("case", [CASES[4], CASES[17]], ids=_ids)
 def test_bulk_grad_return_noalloc(cpt, cuda_device, case, kernel):

@@ -37,9 +37,17 @@ def test_gradient_return_rule(path):
     # shared memory: 2 x (P+1) x row <= 112 KB keeps two CTAs on an SM
     assert path(GR, 8, F32, F32, False, 6368, 1 << 20) == "bulk"
     assert path(GR, 8, F32, F32, False, 6384, 1 << 20) == "loads"
-    # mixed types and accumulate mode always take the 16-byte-load kernel
+    # mixed types take the 16-byte-load kernel
     assert path(GR, 8, BF16, F32, False, 5120, 1 << 20) == "loads"
-    assert path(GR, 8, BF16, BF16, True, 5120, 1 << 20) == "loads"
+    # accumulate mode follows the same rule, its launch counting the owner row
+    assert path(GR, 8, BF16, BF16, True, 5120, 1 << 20) == "bulk"
+    assert path(GR, 4, BF16, BF16, True, 5120, 2 * 262144) == "bulk"
+    assert path(GR, 4, BF16, BF16, True, 2048, 2 * 524288) == "bulk"
+    assert path(GR, 4, BF16, BF16, True, 2048, 2 * 32768) == "loads"   # 0.8 GB
+    # 2 GiB at P=4 with 5 KB rows: 83887 rows overwrite (5 rows each) is just
+    # under it; accumulate (6 rows each) is over it
+    assert path(GR, 4, BF16, BF16, False, 5120, 83886) == "loads"
+    assert path(GR, 4, BF16, BF16, True, 5120, 83886) == "bulk"
 
 
 def test_row_gather_rule(path):
@@ -74,7 +82,8 @@ def test_forced_paths(cpt, path):
     # and nowhere else
     assert path(GR, 8, F32, F32, False, 6384, 10) == "loads"
     assert path(GR, 4, BF16, F32, False, 5120, 10) == "loads"
-    assert path(GR, 4, BF16, BF16, True, 5120, 10) == "loads"
+    assert path(GR, 4, BF16, BF16, True, 5120, 10) == "bulk"   # accumulate, when forced
+    assert path(GR, 4, BF16, F32, True, 5120, 10) == "loads"
     assert path(GATHER, 4, BF16, BF16, False, 51216, 10) == "loads"
     assert path(SLOT, 2, F32, F32, False, 4080, 0) == "loads"
     assert path(SLOT, 2, BF16, F32, False, 1 << 30, 0) == "loads"
