@@ -9,17 +9,17 @@
 //
 // HBM-bound: per output row it reads P input rows and writes one. Two kernels
 // share the arithmetic (binary32 adds in writer order):
-//  - grad_return_bulk_kernel, for equal input and output types, in the
-//    cp_size, row and launch sizes where it measured faster (prefer_bulk;
-//    set_kernel_path overrides the rule), in either mode. Every warp runs its
+//  - grad_return_bulk_kernel, in the cp_size, row and launch sizes where it
+//    measured faster (prefer_bulk; set_kernel_path overrides the rule), for
+//    any input and output types and either mode. Every warp runs its
 //    own row pipeline: lane 0 brings the P writer rows into shared memory
 //    with P bulk copies (cp.async.bulk) counted on one mbarrier, the warp
 //    sums them out of shared memory into a staged output row, and lane 0
 //    writes that row back with one bulk store. Every mbarrier wait has a
 //    time and poll budget; a wait that runs out is counted in
 //    g_wait_timeouts and stops the warp.
-//  - grad_return_kernel, for all other cases (mixed types, short rows, small
-//    launches): a warp owns one output row at a time and each lane keeps
+//  - grad_return_kernel, for all other cases (short rows, small launches,
+//    P <= 2): a warp owns one output row at a time and each lane keeps
 //    U x P 16-byte loads in flight before summing.
 // Both size the grid to whole CTAs per SM and stride over rows in output order.
 #include <atomic>
@@ -50,14 +50,17 @@ constexpr int kBulkMaxSmem = 112 * 1024;      // keeps two CTAs (four warps) on 
 // So for P <= 6 the rule also asks for launches of at least 2 GiB.
 constexpr int64_t kBulkMinLaunchBytes = int64_t(2) << 30;
 
-bool bulk_fits(int P, int64_t row_bytes)
+// Whether the bulk kernel can take rows of these sizes: its stages fit the
+// shared-memory budget, and the output rows (half the input row for float32
+// in, bf16 out) stay whole 16-byte units, as bulk copies need.
+bool bulk_fits(int P, int64_t row_bytes, int64_t out_row_bytes)
 {
-    return (int64_t)kBulkWarps * (P + 1) * row_bytes <= kBulkMaxSmem;
+    return out_row_bytes % 16 == 0 && (int64_t)kBulkWarps * (P * row_bytes + out_row_bytes) <= kBulkMaxSmem;
 }
 
-bool prefer_bulk(int P, int type, int64_t row_bytes, int64_t launch_bytes)
+bool prefer_bulk(int P, int type, int64_t row_bytes, int64_t out_row_bytes, int64_t launch_bytes)
 {
-    if (row_bytes < 1024 || !bulk_fits(P, row_bytes)) return false;
+    if (row_bytes < 1024 || !bulk_fits(P, row_bytes, out_row_bytes)) return false;
     if (P <= 6 && launch_bytes < kBulkMinLaunchBytes) return false;
     if (P >= 5) return true;
     if (P == 4) return type == kBf16 ? row_bytes >= 2048 : row_bytes <= 2048;
@@ -207,19 +210,52 @@ __global__ void __launch_bounds__(kThreads) grad_return_kernel(const GradReturnP
     }
 }
 
+// One output unit (the E elements of a 16-byte input unit) in shared memory:
+// read back as binary32, or written from binary32 with one rounding for bf16.
+template <int OUT, int E>
+__device__ __forceinline__ void widen_out(const uint8_t *p, float (&a)[E])
+{
+    if constexpr (OUT == kBf16) {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(p);
+#pragma unroll
+        for (int h = 0; h < E / 2; ++h) {
+            a[2 * h] = bf16_lo(w[h]);
+            a[2 * h + 1] = bf16_hi(w[h]);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) a[e] = reinterpret_cast<const float *>(p)[e];
+    }
+}
+
+template <int OUT, int E>
+__device__ __forceinline__ void pack_out(uint8_t *p, const float (&a)[E])
+{
+    if constexpr (OUT == kBf16) {
+        uint32_t *w = reinterpret_cast<uint32_t *>(p);
+#pragma unroll
+        for (int h = 0; h < E / 2; ++h) w[h] = pack_bf16x2(a[2 * h], a[2 * h + 1]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) reinterpret_cast<float *>(p)[e] = a[e];
+    }
+}
+
 // Same-type overwrite case through shared memory. Per warp: a stage of P
 // input rows and one output row. Lane 0 issues the loads of a row while the
 // map entry of the row after it is already being fetched.
-template <int P, int T, bool ACC>
+template <int P, int IN, int OUT, bool ACC>
 __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const GradReturnParams p)
 {
-    constexpr int E = Unit<T>::kElems;
+    constexpr int E = Unit<IN>::kElems;
+    constexpr int kOutUnitBytes = E * (OUT == kBf16 ? 2 : 4);
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kBulkWarps];
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
-    const int rb = p.in_row_bytes;  // equals out_row_bytes: same element type
-    uint8_t *stage = smem + (size_t)wid * (P + 1) * rb;
+    const int rb = p.in_row_bytes;
+    const int ob = p.out_row_bytes;
+    uint8_t *stage = smem + (size_t)wid * ((size_t)P * rb + ob);
     uint8_t *out = stage + (size_t)P * rb;
     uint64_t *bar = bars + wid;
     if (lane == 0) {
@@ -244,13 +280,13 @@ __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const
             // accumulate mode reloads `out` with the owner's current row: the
             // previous row's store must have read it first
             if constexpr (ACC) bulk_wait_read<0>();
-            mbar_expect_tx(bar, (uint32_t)((P + (ACC ? 1 : 0)) * rb) + stall);
+            mbar_expect_tx(bar, (uint32_t)(P * rb + (ACC ? ob : 0)) + stall);
 #pragma unroll
             for (int w = 0; w < P; ++w)
                 bulk_load(stage + (size_t)w * rb, (t ? p.w[1][w] : p.w[0][w]) + g * rb, (uint32_t)rb,
                           bar);
             if constexpr (ACC)
-                bulk_load(out, (t ? p.o[1][o] : p.o[0][o]) + j * p.out_row_bytes, (uint32_t)rb, bar);
+                bulk_load(out, (t ? p.o[1][o] : p.o[0][o]) + j * ob, (uint32_t)ob, bar);
             const int64_t Rn = R + stride;
             if (Rn < p.rows) g_next = __ldg(p.l2g + p.q0 + (Rn >= p.T ? Rn - p.T : Rn));
         }
@@ -266,38 +302,35 @@ __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const
         if (!ACC && lane == 0) bulk_wait_read<0>();  // the previous row's store has read `out`
         __syncwarp();
         for (int u = lane; u < p.units; u += 32) {
+            uint8_t *ou = out + (size_t)u * kOutUnitBytes;
             float acc[E];
             // overwrite: start from writer 0; accumulate: from the owner's value
-            Unit<T>::widen(*reinterpret_cast<const uint4 *>((ACC ? out : stage) + (size_t)u * 16), acc);
+            if constexpr (ACC) {
+                widen_out<OUT>(ou, acc);
+            } else {
+                Unit<IN>::widen(*reinterpret_cast<const uint4 *>(stage + (size_t)u * 16), acc);
+            }
 #pragma unroll
             for (int w = ACC ? 0 : 1; w < P; ++w) {
                 float x[E];
-                Unit<T>::widen(*reinterpret_cast<const uint4 *>(stage + (size_t)w * rb + (size_t)u * 16), x);
+                Unit<IN>::widen(*reinterpret_cast<const uint4 *>(stage + (size_t)w * rb + (size_t)u * 16), x);
 #pragma unroll
                 for (int e = 0; e < E; ++e) acc[e] = add_rn(acc[e], x[e]);
             }
-            uint4 v;
-            if constexpr (T == kBf16) {
-                v = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-            } else {
-                v = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
-                               __float_as_uint(acc[2]), __float_as_uint(acc[3]));
-            }
-            *reinterpret_cast<uint4 *>(out + (size_t)u * 16) = v;
+            pack_out<OUT>(ou, acc);
         }
         fence_proxy_async_smem();  // the row's generic writes before the bulk store reads it
         __syncwarp();
-        if (lane == 0) bulk_store((t ? p.o[1][o] : p.o[0][o]) + j * p.out_row_bytes, out, (uint32_t)rb);
+        if (lane == 0) bulk_store((t ? p.o[1][o] : p.o[0][o]) + j * ob, out, (uint32_t)ob);
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
 }
 
-template <int P, int T, bool ACC>
+template <int P, int IN, int OUT, bool ACC>
 cudaError_t launch_bulk(const GradReturnParams &p, size_t smem, cudaStream_t stream)
 {
-    auto kernel = grad_return_bulk_kernel<P, T, ACC>;
+    auto kernel = grad_return_bulk_kernel<P, IN, OUT, ACC>;
     // Per device: whether the shared-memory limit is raised, and the
     // occupancy of the last shared-memory size asked for, packed into one
     // word as (smem << 8) | CTAs per SM so that concurrent callers never pair
@@ -332,10 +365,9 @@ cudaError_t launch_bulk(const GradReturnParams &p, size_t smem, cudaStream_t str
 template <int P, int IN, int OUT, bool ACC>
 cudaError_t launch_typed(const GradReturnParams &p, cudaStream_t stream)
 {
-    if constexpr (IN == OUT) {
-        if (grad_return_uses_bulk(P, IN, OUT, ACC, p.in_row_bytes, p.rows))
-            return launch_bulk<P, IN, ACC>(p, (size_t)kBulkWarps * (P + 1) * p.in_row_bytes, stream);
-    }
+    if (grad_return_uses_bulk(P, IN, OUT, ACC, p.in_row_bytes, p.rows))
+        return launch_bulk<P, IN, OUT, ACC>(
+            p, (size_t)kBulkWarps * ((size_t)P * p.in_row_bytes + p.out_row_bytes), stream);
     constexpr int U = P <= 4 ? 2 : 1;
     auto kernel = grad_return_kernel<P, IN, OUT, U, ACC>;
     static std::atomic<int> blocks_per_sm[64];  // per device, one table per instantiation
@@ -386,16 +418,21 @@ cudaError_t launch_acc(const GradReturnParams &p, int cp_size, int in, int out, 
 bool grad_return_uses_bulk(int P, int in_dtype, int out_dtype, bool accumulate, int64_t row_bytes,
                            int64_t rows)
 {
-    if (in_dtype != out_dtype) return false;
+    const int64_t out_row_bytes = row_bytes / (in_dtype == kBf16 ? 2 : 4) * (out_dtype == kBf16 ? 2 : 4);
     const int choice = g_kernel_choice.load(std::memory_order_relaxed);
-    if (choice == 2) return bulk_fits(P, row_bytes);
-    // the same rule serves both modes; accumulate also reads the owner row.
-    // Measured in accumulate mode on GB300 (L2 flushed / warm): -4.5 % / 0 %
-    // at P=4 with 5 KB rows (16 GB), -7 % / -1 % at P=8, -5 % / -1 % at P=4
-    // with 2 KB rows (6.7 GB), and +4 % at P=4 with 2 KB rows in a 0.8 GB
-    // launch, which the launch-size condition sends to the loads kernel.
-    const int64_t launch_bytes = rows * (P + (accumulate ? 2 : 1)) * row_bytes;
-    return choice == 0 && prefer_bulk(P, in_dtype, row_bytes, launch_bytes);
+    if (choice == 2) return bulk_fits(P, row_bytes, out_row_bytes);
+    // One rule for both modes and for mixed types, keyed on the input rows;
+    // the launch counts the output rows at their own width (twice in
+    // accumulate mode, which reads them back). Measured on GB300, L2 flushed /
+    // warm, against the 16-byte-load kernel:
+    //  - accumulate, equal types: -4.5 % / 0 % at P=4 with 5 KB rows (16 GB),
+    //    -7 % / -1 % at P=8, -5 % / -1 % at P=4 with 2 KB rows (6.7 GB), and
+    //    +4 % at P=4 with 2 KB rows in a 0.8 GB launch (left to loads);
+    //  - bf16 writers into float32 owners: -10 % / -7 % overwrite and
+    //    -38 % / -12 % accumulate at P=4 with 5 KB rows; even at P=8; -4 % /
+    //    +2 % overwrite and -41 % / -16 % accumulate at P=4 with 2 KB rows.
+    const int64_t launch_bytes = rows * (P * row_bytes + (accumulate ? 2 : 1) * out_row_bytes);
+    return choice == 0 && prefer_bulk(P, in_dtype, row_bytes, out_row_bytes, launch_bytes);
 }
 
 void set_kernel_path(int choice)

@@ -384,17 +384,18 @@ CPT_API cpt_status cpt_grad_return_accumulate(const cpt_plan *plan, const void *
  *    per contiguous source run and one bulk store per rank piece; it needs
  *    4 blocks to fit in 200 KB. Gradient return: one owner row's P writer
  *    rows per warp (and, for cpt_grad_return_accumulate, the owner's current
- *    row); it needs equal input and output types and 2 x (P+1) x row bytes
- *    of at most 112 KB. Slot reduce: 4 KB of every slot per warp; it needs equal input
+ *    row); it needs 2 x (P x input row + output row) bytes of at most
+ *    112 KB. Slot reduce: 4 KB of every slot per warp; it needs equal input
  *    and output types, and sums its last partial 4 KB with the loads
  *    kernel. Where a condition fails, the loads kernel runs.
  *  - CPT_KERNEL_AUTO (the default): bulk where it measured faster on GB300,
  *    loads elsewhere.
  *    Row gather: rows of at least 2 KB in launches that move at least
  *    384 MiB.
- *    Gradient return, either mode: rows of at least 1 KB, and for P <= 6
- *    launches of at least 2 GiB (counting the owner row read back in
- *    accumulate mode), with these row sizes per P:
+ *    Gradient return, either mode and any types: input rows of at least
+ *    1 KB, and for P <= 6 launches of at least 2 GiB (output rows counted at
+ *    their own width, twice in accumulate mode), with these input row sizes
+ *    per P (by the input type):
  *      P >= 5: any row size;
  *      P = 4:  bf16 rows of at least 2 KB, float32 rows of at most 2 KB;
  *      P = 3:  bf16 rows of at least 3 KB;

@@ -168,6 +168,59 @@ def test_bulk_grad_return_accumulate(cpt, cuda_device, case, kernel):
             assert np.array_equal(bits(got[o]), bits(want[o])), f"owner {o}"
 
 
+MIXED = [
+    (DSC, 4, [8, 56, 200], 2560, "bf16", "f32"),     # bf16 writers into float32 owners
+    (DSC, 8, [16, 48], 1024, "bf16", "f32"),
+    (DSC, 4, [8, 56, 200], 1280, "f32", "bf16"),     # float32 writers into bf16 owners
+    (PADDED, 3, [5, 33, 1, 12], 512, "f32", "bf16"),
+    (PACKED, 5, [0, 77, 23], 520, "bf16", "f32"),
+]
+
+
+@pytest.mark.parametrize("kernel", KERNELS, indirect=True)
+@pytest.mark.parametrize("accumulate", [False, True], ids=["overwrite", "accumulate"])
+@pytest.mark.parametrize("case", MIXED, ids=lambda c: f"L{c[0]}-P{c[1]}-row{c[3]}-{c[4]}to{c[5]}")
+def test_bulk_grad_return_mixed_types(cpt, cuda_device, case, accumulate, kernel):
+    """Writers and owners of different element types; the bulk kernel stages
+    output rows of the output type."""
+    layout, P, lens, row, din, dout = case
+    cu = synth.cu_from_lengths(lens)
+    T = int(cu[-1])
+    if layout == PADDED:
+        cup, l2g, _ = oracle.padded_index_map(P, cu)
+        Tpad = int(cup[-1])
+    else:
+        l2g, _ = oracle.index_map(layout, P, cu, T)
+        Tpad = T
+    rng = np.random.default_rng(7700 + P + row)
+    gin = synth.uniform_f32 if din == "f32" else synth.uniform_bf16
+    gout = synth.uniform_f32 if dout == "f32" else synth.uniform_bf16
+    wk = [gin(rng, (Tpad, row)) for _ in range(P)]
+    wv = [gin(rng, (Tpad, row)) for _ in range(P)]
+    plan = cpt.cpt_plan_create(layout, P, cu, T)
+    code = oracle.F32 if dout == "f32" else oracle.BF16
+    if accumulate:
+        sk = [gout(rng, (Tpad // P, row)) for _ in range(P)]
+        sv = [gout(rng, (Tpad // P, row)) for _ in range(P)]
+        ok = torch.stack([to_dev(x) for x in sk])
+        ov = torch.stack([to_dev(x) for x in sv])
+        cpt.cpt_grad_return_accumulate(plan, torch.stack([to_dev(w) for w in wk]),
+                                       torch.stack([to_dev(w) for w in wv]), ok, ov)
+        wants = (oracle.grad_return_accumulate(l2g, wk, sk), oracle.grad_return_accumulate(l2g, wv, sv))
+    else:
+        odt = torch.float32 if dout == "f32" else torch.bfloat16
+        ok = torch.empty((P, Tpad // P, row), dtype=odt, device="cuda")
+        ov = torch.empty_like(ok)
+        cpt.cpt_grad_return(plan, torch.stack([to_dev(w) for w in wk]), torch.stack([to_dev(w) for w in wv]),
+                            ok, ov)
+        wants = (oracle.grad_return(l2g, wk, code), oracle.grad_return(l2g, wv, code))
+    torch.cuda.synchronize()
+    for want, out in zip(wants, (ok, ov)):
+        got = to_host(out)
+        for o in range(P):
+            assert np.array_equal(bits(got[o]), bits(want[o])), f"owner {o}"
+
+
 @pytest.mark.parametrize("kernel", ["loads", "bulk"], indirect=True)
 @pytest.mark.parametrize("case", [CASES[4], CASES[17]], ids=_ids)
 def test_bulk_grad_return_noalloc(cpt, cuda_device, case, kernel):

@@ -37,8 +37,11 @@ def test_gradient_return_rule(path):
     # shared memory: 2 x (P+1) x row <= 112 KB keeps two CTAs on an SM
     assert path(GR, 8, F32, F32, False, 6368, 1 << 20) == "bulk"
     assert path(GR, 8, F32, F32, False, 6384, 1 << 20) == "loads"
-    # mixed types take the 16-byte-load kernel
-    assert path(GR, 8, BF16, F32, False, 5120, 1 << 20) == "loads"
+    # mixed types follow the same rule, keyed on the input rows
+    assert path(GR, 4, BF16, F32, False, 5120, 2 * 262144) == "bulk"
+    assert path(GR, 4, BF16, F32, True, 2048, 2 * 524288) == "bulk"
+    assert path(GR, 2, BF16, F32, True, 5120, 2 * 262144) == "loads"
+    assert path(GR, 8, BF16, F32, False, 8192, 1 << 20) == "loads"  # 2 x (8 x 8 + 16) KB > 112 KB
     # accumulate mode follows the same rule, its launch counting the owner row
     assert path(GR, 8, BF16, BF16, True, 5120, 1 << 20) == "bulk"
     assert path(GR, 4, BF16, BF16, True, 5120, 2 * 262144) == "bulk"
@@ -81,9 +84,10 @@ def test_forced_paths(cpt, path):
     assert path(SLOT, 2, F32, F32, False, 4096, 0) == "bulk"
     # and nowhere else
     assert path(GR, 8, F32, F32, False, 6384, 10) == "loads"
-    assert path(GR, 4, BF16, F32, False, 5120, 10) == "loads"
     assert path(GR, 4, BF16, BF16, True, 5120, 10) == "bulk"   # accumulate, when forced
-    assert path(GR, 4, BF16, F32, True, 5120, 10) == "loads"
+    assert path(GR, 4, BF16, F32, False, 5120, 10) == "bulk"   # mixed types, when forced
+    assert path(GR, 4, BF16, F32, True, 5120, 10) == "bulk"
+    assert path(GR, 8, BF16, F32, False, 8192, 10) == "loads"  # 2 x (8 x 8 + 16) KB > 112 KB
     assert path(GATHER, 4, BF16, BF16, False, 51216, 10) == "loads"
     assert path(SLOT, 2, F32, F32, False, 4080, 0) == "loads"
     assert path(SLOT, 2, BF16, F32, False, 1 << 30, 0) == "loads"
