@@ -128,26 +128,42 @@ __device__ __forceinline__ void store_unit(uint8_t *p, const float (&a)[E])
     }
 }
 
-// Widen the current owner values of one unit (ACC mode). A coherent
-// streaming load: this thread overwrites the same bytes afterwards.
+// The current owner values of one unit (ACC mode), loaded raw so that the
+// load can be issued with the writer loads and widened after they land:
+// E output elements, 8, 16 or 32 bytes. Coherent streaming loads: this
+// thread overwrites the same bytes afterwards.
 template <int OUT, int E>
-__device__ __forceinline__ void load_unit(const uint8_t *p, float (&a)[E])
+struct OwnerUnit {
+    uint4 r[(E * (OUT == kBf16 ? 2 : 4) + 15) / 16];
+};
+
+template <int OUT, int E>
+__device__ __forceinline__ void load_owner(const uint8_t *p, OwnerUnit<OUT, E> &o)
+{
+    if constexpr (OUT == kBf16 && E == 4) {
+        const uint2 v = __ldcs(reinterpret_cast<const uint2 *>(p));
+        o.r[0] = make_uint4(v.x, v.y, 0u, 0u);
+    } else {
+#pragma unroll
+        for (int h = 0; h < (int)(sizeof(o.r) / 16); ++h) o.r[h] = __ldcs(reinterpret_cast<const uint4 *>(p) + h);
+    }
+}
+
+template <int OUT, int E>
+__device__ __forceinline__ void widen_owner(const OwnerUnit<OUT, E> &o, float (&a)[E])
 {
     if constexpr (OUT == kBf16) {
-        if constexpr (E == 8) {
-            const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p));
-            a[0] = bf16_lo(v.x); a[1] = bf16_hi(v.x); a[2] = bf16_lo(v.y); a[3] = bf16_hi(v.y);
-            a[4] = bf16_lo(v.z); a[5] = bf16_hi(v.z); a[6] = bf16_lo(v.w); a[7] = bf16_hi(v.w);
-        } else {
-            const uint2 v = __ldcs(reinterpret_cast<const uint2 *>(p));
-            a[0] = bf16_lo(v.x); a[1] = bf16_hi(v.x); a[2] = bf16_lo(v.y); a[3] = bf16_hi(v.y);
+        const uint32_t w[4] = {o.r[0].x, o.r[0].y, o.r[0].z, o.r[0].w};
+#pragma unroll
+        for (int h = 0; h < E / 2; ++h) {
+            a[2 * h] = bf16_lo(w[h]);
+            a[2 * h + 1] = bf16_hi(w[h]);
         }
     } else {
 #pragma unroll
-        for (int h = 0; h < E; h += 4) {
-            const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p + h * 4));
-            a[h] = __uint_as_float(v.x); a[h + 1] = __uint_as_float(v.y);
-            a[h + 2] = __uint_as_float(v.z); a[h + 3] = __uint_as_float(v.w);
+        for (int h = 0; h < E / 4; ++h) {
+            a[4 * h] = __uint_as_float(o.r[h].x); a[4 * h + 1] = __uint_as_float(o.r[h].y);
+            a[4 * h + 2] = __uint_as_float(o.r[h].z); a[4 * h + 3] = __uint_as_float(o.r[h].w);
         }
     }
 }
@@ -177,12 +193,14 @@ __global__ void __launch_bounds__(kThreads) grad_return_kernel(const GradReturnP
 
         for (int u0 = lane; u0 < units; u0 += 32 * U) {
             uint4 v[U][P];
+            OwnerUnit<OUT, E> own[U];
 #pragma unroll
             for (int k = 0; k < U; ++k) {
                 const int u = u0 + 32 * k;
                 if (u < units) {
 #pragma unroll
                     for (int w = 0; w < P; ++w) v[k][w] = ld_once(src[w] + (int64_t)u * 16);
+                    if constexpr (ACC) load_owner<OUT, E>(dst + (int64_t)u * kOutUnitBytes, own[k]);
                 }
             }
 #pragma unroll
@@ -192,7 +210,7 @@ __global__ void __launch_bounds__(kThreads) grad_return_kernel(const GradReturnP
                     uint8_t *out = dst + (int64_t)u * kOutUnitBytes;
                     float acc[E];
                     if constexpr (ACC) {
-                        load_unit<OUT>(out, acc);
+                        widen_owner<OUT, E>(own[k], acc);
                     } else {
                         Unit<IN>::widen(v[k][0], acc);
                     }
