@@ -259,9 +259,10 @@ __device__ __forceinline__ void pack_out(uint8_t *p, const float (&a)[E])
     }
 }
 
-// Same-type overwrite case through shared memory. Per warp: a stage of P
-// input rows and one output row. Lane 0 issues the loads of a row while the
-// map entry of the row after it is already being fetched.
+// Any input and output types, either mode, through shared memory. Per warp:
+// a stage of P input rows and one output row (which holds the owner's current
+// row in accumulate mode). Lane 0 issues the loads of a row while the map
+// entry of the row after it is already being fetched.
 template <int P, int IN, int OUT, bool ACC>
 __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const GradReturnParams p)
 {
@@ -443,12 +444,12 @@ bool grad_return_uses_bulk(int P, int in_dtype, int out_dtype, bool accumulate, 
     // the launch counts the output rows at their own width (twice in
     // accumulate mode, which reads them back). Measured on GB300, L2 flushed /
     // warm, against the 16-byte-load kernel:
-    //  - accumulate, equal types: -4.5 % / 0 % at P=4 with 5 KB rows (16 GB),
-    //    -7 % / -1 % at P=8, -5 % / -1 % at P=4 with 2 KB rows (6.7 GB), and
-    //    +4 % at P=4 with 2 KB rows in a 0.8 GB launch (left to loads);
-    //  - bf16 writers into float32 owners: -10 % / -7 % overwrite and
-    //    -38 % / -12 % accumulate at P=4 with 5 KB rows; even at P=8; -4 % /
-    //    +2 % overwrite and -41 % / -16 % accumulate at P=4 with 2 KB rows.
+    //  - accumulate, equal types: 0 % / +2 % at P=4 with 5 KB rows (16 GB),
+    //    -9 % / -4 % at P=8, -1.5 % / +1 % at P=4 with 2 KB rows (6.7 GB),
+    //    and +8 % at P=4 with 2 KB rows in a 0.8 GB launch (left to loads);
+    //  - bf16 writers into float32 owners: -10 % / -6 % overwrite and
+    //    -2 % / +2 % accumulate at P=4 with 5 KB rows; even at P=8; -4 % /
+    //    +2 % overwrite and -5.5 % / -3 % accumulate at P=4 with 2 KB rows.
     const int64_t launch_bytes = rows * (P * row_bytes + (accumulate ? 2 : 1) * out_row_bytes);
     return choice == 0 && prefer_bulk(P, in_dtype, row_bytes, out_row_bytes, launch_bytes);
 }
