@@ -25,7 +25,9 @@ pytestmark = pytest.mark.gpu
 DSC, PACKED, PADDED = 0, 1, 3
 
 # (layout, P, document lengths, row elements, element type); the comment
-# names the kernel the library picks for the case
+# names the kernel that the row-size part of the rule picks. These launches
+# are small, so under "auto" the launch-size part (at least 2 GiB for P <= 6)
+# keeps P <= 6 on the 16-byte loads; the forced runs cover both kernels.
 CASES = [
     (DSC, 1, [64, 32], 2560, "bf16"),        # 16-byte loads: P = 1
     (DSC, 2, [40, 24], 2560, "bf16"),        # 16-byte loads: P = 2
