@@ -4,9 +4,11 @@ call of the C ABI, each output compared with the oracle bit for bit.
 Each case draws a layout, P in 1..8, a document mix (zero-length documents
 included), a row width that is a multiple of 16 bytes but not of a warp's
 512 bytes, and a dtype pair, and runs once under the measured kernel rule
-and once with the bulk-copy gradient return forced. The fixed cases
-elsewhere pin known corners; this sweep looks for the corners nobody
-thought of.
+and once with the bulk-copy kernels forced. A second, wider sweep draws up to
+40 documents, batches of up to about 10^6 tokens and rows of up to 4096
+elements (16 KB of float32), and runs each case with either kernel family
+forced. The fixed cases elsewhere pin known corners; these sweeps look for
+the corners nobody thought of.
 """
 import numpy as np
 import pytest
@@ -41,6 +43,32 @@ def _case(seed):
     return rng, layout, P, lens, row, str(din), str(dout)
 
 
+def _wide_case(seed):
+    """Longer batches and wider rows: many bulk-copy blocks and row
+    pipelines per case, runs of source rows across block edges, and blocks
+    split across rank pieces. About 64 MB of writer rows at most."""
+    rng = np.random.default_rng(77000 + seed)
+    layout = int(rng.choice([DSC, PACKED, PADDED]))
+    P = int(rng.integers(1, 9))
+    n = int(rng.integers(1, 41))
+    din = str(rng.choice(["f32", "bf16"]))
+    dout = str(rng.choice(["f32", "bf16"]))
+    lo, hi = [(1, 41), (40, 161), (160, 513)][int(rng.integers(0, 3))]
+    row = int(rng.integers(lo, hi)) * 8
+    esz = 4 if din == "f32" else 2
+    max_T = max(2 * P * n, (48 << 20) // (row * esz * (P + 1)))
+    per = max(1, max_T // n)
+    if layout == DSC:
+        lens = (rng.integers(0, max(2, per // (2 * P)) + 1, size=n) * 2 * P).tolist()
+    else:
+        lens = rng.integers(0, per + 1, size=n).tolist()
+    if layout == PACKED:
+        lens[-1] += (-sum(lens)) % P
+    if sum(lens) == 0:
+        lens[0] = 2 * P
+    return rng, layout, P, lens, row, din, dout
+
+
 def _rand(rng, shape, dt):
     return synth.uniform_f32(rng, shape) if dt == "f32" else synth.uniform_bf16(rng, shape)
 
@@ -52,9 +80,8 @@ def _tdt(dt):
 @pytest.fixture(params=["auto", "bulk"])
 def kernel_path(cpt, request):
     """Each case runs under the measured kernel rule, and again with the
-    bulk-copy gradient return forced wherever it can run (equal types,
-    overwrite mode), so that kernel also meets rows of any width from 16
-    bytes up."""
+    bulk-copy kernels forced wherever they can run, so that they also meet
+    rows of any width from 16 bytes up."""
     cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO if request.param == "auto"
                                    else cpt.CPT_KERNEL_BULK)
     yield request.param
@@ -63,7 +90,24 @@ def kernel_path(cpt, request):
 
 @pytest.mark.parametrize("seed", range(100))
 def test_random_case_every_call(cpt, cuda_device, seed, kernel_path):
-    rng, layout, P, lens, row, din, dout = _case(seed)
+    _run_case(cpt, seed, _case(seed))
+
+
+@pytest.fixture(params=["loads", "bulk"])
+def forced_path(cpt, request):
+    """One kernel family forced for the whole case, then the default back."""
+    cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_LOADS if request.param == "loads" else cpt.CPT_KERNEL_BULK)
+    yield request.param
+    cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_wide_random_case_every_call(cpt, cuda_device, seed, forced_path):
+    _run_case(cpt, seed, _wide_case(seed))
+
+
+def _run_case(cpt, seed, case):
+    rng, layout, P, lens, row, din, dout = case
     cu = synth.cu_from_lengths(lens)
     T = int(cu[-1])
     n = len(lens)
