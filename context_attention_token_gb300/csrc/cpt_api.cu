@@ -237,6 +237,7 @@ struct cpt_plan {
     const uint8_t *ws;
     size_t ws_bytes;
     int32_t *cu, *cup, *cu_local, *num_segs, *first, *offs, *l2g, *g2l, *l2r, *r2l;
+    std::vector<int32_t> h_cu;   // host copy of cu_seqlens (the source of its device copy)
     std::vector<int32_t> h_cup;  // host copy of the padded boundaries
 };
 
@@ -375,6 +376,16 @@ cpt_status cpt_plan_create(cpt_layout layout, int32_t P, const int32_t *cu, int3
     if (p == nullptr) return fail(CPT_ERR_INVALID_ARG, "out of host memory");
     uint8_t *base = static_cast<uint8_t *>(workspace);
     const bool pad = is_padded(layout);
+    // The device copies below read plan-owned pageable vectors, which the
+    // copy stages before returning, so the caller may reuse cu_seqlens (even
+    // pinned memory, whose copy would otherwise still be in flight) at once.
+    try {
+        p->h_cu.assign(cu, cu + (size_t)n + 1);
+        if (pad) p->h_cup.resize((size_t)n + 1);
+    } catch (const std::bad_alloc &) {
+        delete p;
+        return fail(CPT_ERR_INVALID_ARG, "out of host memory");
+    }
     p->layout = layout;
     p->map_layout = pad ? (int)CPT_LAYOUT_DUAL_CHUNK_SWAP : (int)layout;
     p->P = P;
@@ -392,12 +403,6 @@ cpt_status cpt_plan_create(cpt_layout layout, int32_t P, const int32_t *cu, int3
     p->g2l = reinterpret_cast<int32_t *>(base + w.g2l);
     if (pad) {
         // every document padded up to a multiple of 2P
-        try {
-            p->h_cup.resize((size_t)n + 1);
-        } catch (const std::bad_alloc &) {
-            delete p;
-            return fail(CPT_ERR_INVALID_ARG, "out of host memory");
-        }
         p->h_cup[0] = 0;
         for (int32_t i = 0; i < n; ++i) {
             const int32_t L = cu[i + 1] - cu[i];
@@ -416,7 +421,7 @@ cpt_status cpt_plan_create(cpt_layout layout, int32_t P, const int32_t *cu, int3
     p->Tp = p->Tpad / P;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemcpyAsync(p->cu, cu, sizeof(int32_t) * (size_t)(n + 1),
+    cudaError_t e = cudaMemcpyAsync(p->cu, p->h_cu.data(), sizeof(int32_t) * (size_t)(n + 1),
                                     cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess && pad)
         e = cudaMemcpyAsync(p->cup, p->h_cup.data(), sizeof(int32_t) * (size_t)(n + 1),
@@ -1103,7 +1108,8 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
     Trace trace("cpt_grad_return_noalloc");
     cpt_status st = cpt_validate_layout(layout, P, cu, n, T);
     if (st) return st;
-    // the padded layout is the per-document one over padded boundaries
+    // the padded layout is the per-document one over padded boundaries; the
+    // other layouts copy cu_seqlens into the same vector before the upload
     std::vector<int32_t> cup;
     const int32_t *cu_map = cu;
     int64_t Tmap = T;
@@ -1169,6 +1175,16 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
     // scratch has to start at zero
     int32_t *d_cu = scratch;
     int32_t *d_l2g = scratch + kNoAllocCuSlots;
+    // copy from a pageable host vector, which the copy stages before
+    // returning, so the caller may reuse cu_seqlens (even pinned) at once
+    if (!is_padded(layout)) {
+        try {
+            cup.assign(cu, cu + (size_t)n + 1);
+        } catch (const std::bad_alloc &) {
+            return fail(CPT_ERR_INVALID_ARG, "out of host memory");
+        }
+        cu_map = cup.data();
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemcpyAsync(d_cu, cu_map, sizeof(int32_t) * (size_t)(n + 1),
                                     cudaMemcpyHostToDevice, s);

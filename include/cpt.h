@@ -195,6 +195,9 @@ CPT_API size_t cpt_plan_workspace_bytes(cpt_layout layout, int32_t cp_size, int3
  * partition and gradient return always see the same policy ([TE-3221]
  * "Scope and constraints": partition and attention must see the same
  * selection).
+ *  cu_seqlens_host  as for cpt_validate_layout; copied before the call
+ *                   returns, so the caller may reuse or free it at once
+ *                   (pinned host memory included).
  *  workspace        device, 256-byte aligned, >= cpt_plan_workspace_bytes;
  *                   owned by the caller, must outlive the plan and every
  *                   call that uses it.
