@@ -1006,7 +1006,7 @@ cpt_status cpt_set_kernel_path(cpt_kernel_path kernel)
 {
     Trace trace("cpt_set_kernel_path");
     if (kernel != CPT_KERNEL_AUTO && kernel != CPT_KERNEL_LOADS && kernel != CPT_KERNEL_BULK)
-        return fail(CPT_ERR_INVALID_ARG, "unknown gradient return kernel %d", (int)kernel);
+        return fail(CPT_ERR_INVALID_ARG, "unknown kernel path %d (expected AUTO, LOADS or BULK)", (int)kernel);
     set_kernel_path((int)kernel);
     return CPT_OK;
 }
