@@ -183,7 +183,7 @@ class _Parts:
     contiguous [parts, ...] tensor or as a sequence of tensors, with the
     shape and dtype of one part."""
 
-    __slots__ = ("ptrs", "shape", "dtype")
+    __slots__ = ("ptrs", "shape", "dtype", "part_bytes")
 
     def __init__(self, t, parts: int):
         if isinstance(t, torch.Tensor):
@@ -196,13 +196,18 @@ class _Parts:
             self.ptrs = [base + i * step for i in range(parts)]
             self.shape = tuple(t.shape[1:])
             self.dtype = t.dtype
+            self.part_bytes = step
         else:
             t = list(t)
             if len(t) != parts:
                 raise ValueError(f"expected {parts} tensors, got {len(t)}")
+            for x in t[1:]:
+                if tuple(x.shape) != tuple(t[0].shape) or x.dtype != t[0].dtype:
+                    raise ValueError("the parts differ in shape or dtype")
             self.ptrs = [_ptr(x) for x in t]
             self.shape = tuple(t[0].shape)
             self.dtype = t[0].dtype
+            self.part_bytes = _nbytes(t[0])
 
     def array(self):
         return ctypes.cast((_vp * len(self.ptrs))(*self.ptrs), _vp)
@@ -219,6 +224,48 @@ class _Parts:
         if self.dtype == torch.bfloat16:
             return CPT_BF16
         raise TypeError(f"unsupported dtype {self.dtype} (float32 or bfloat16)")
+
+
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+def _need(t, nbytes: int, what: str, dtype=None):
+    """Refuse a buffer smaller than the bytes the call will touch (the C ABI
+    sees only its address), or of the wrong element type."""
+    if t is None:
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what} has dtype {t.dtype}, expected {dtype}")
+    if _nbytes(t) < nbytes:
+        raise ValueError(f"{what} holds {_nbytes(t)} bytes but the call touches {nbytes}")
+
+
+def _need_parts(parts, rows: int, row_elems: int, what: str):
+    """Every part of `parts` must hold `rows` rows of `row_elems` elements."""
+    if parts is None:
+        return
+    if parts.row_elems() != row_elems:
+        raise ValueError(f"{what} rows have {parts.row_elems()} elements, expected {row_elems}")
+    need = rows * row_elems * torch.tensor([], dtype=parts.dtype).element_size()
+    if parts.part_bytes < need:
+        raise ValueError(f"each part of {what} holds {parts.part_bytes} bytes but the call touches {need}")
+
+
+def _same_kind(ts, what: str):
+    """Tensors of one call that must share dtype and row width."""
+    for t in ts[1:]:
+        if t.dtype != ts[0].dtype or _row_elems(t) != _row_elems(ts[0]):
+            raise ValueError(f"the {what} tensors differ in dtype or row width")
+
+
+def _padded_total(layout: int, cp_size: int, cu_vals) -> int:
+    """Tokens after per-document padding to multiples of 2*cp_size (padded
+    layout), else the total."""
+    if layout != CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED:
+        return int(cu_vals[-1]) if len(cu_vals) else 0
+    m = 2 * cp_size
+    return sum((int(b) - int(a) + m - 1) // m * m for a, b in zip(cu_vals[:-1], cu_vals[1:]))
 
 
 def _cu_array(cu_seqlens):
@@ -299,14 +346,22 @@ def cpt_plan_padded_tokens(plan: Plan) -> int:
 
 def cpt_thd_real_lengths(plan: Plan, real_len: torch.Tensor, stream=None):
     """real_len[r][i] ([P, n] int32) = real tokens of document i on rank r."""
+    _need(real_len, 4 * plan.cp_size * plan.n_docs, "real_len", torch.int32)
     _check(_lib.cpt_thd_real_lengths(plan.handle, _ptr(real_len), _stream(stream)))
 
 
 def cpt_index_map(plan: Plan, l2g: torch.Tensor, g2l: torch.Tensor | None = None, stream=None):
+    _need(l2g, 4 * plan.padded_tokens, "l2g", torch.int32)
+    _need(g2l, 4 * plan.padded_tokens, "g2l", torch.int32)
     _check(_lib.cpt_index_map(plan.handle, _ptr(l2g), _ptr(g2l), _stream(stream)))
 
 
 def cpt_thd_metadata(plan: Plan, num_segs, seg_doc_first, cu_local, seg_offsets, stream=None):
+    P = plan.cp_size
+    _need(num_segs, 4 * P, "num_segs", torch.int32)
+    _need(seg_doc_first, 4 * P, "seg_doc_first", torch.int32)
+    _need(cu_local, 4 * P * (plan.n_docs + 1), "cu_local", torch.int32)
+    _need(seg_offsets, 4 * (P + 1), "seg_offsets", torch.int32)
     _check(_lib.cpt_thd_metadata(plan.handle, _ptr(num_segs), _ptr(seg_doc_first), _ptr(cu_local),
                                  _ptr(seg_offsets), _stream(stream)))
 
@@ -314,8 +369,7 @@ def cpt_thd_metadata(plan: Plan, num_segs, seg_doc_first, cu_local, seg_offsets,
 def cpt_partition(plan: Plan, srcs, dsts, stream=None):
     """dsts[t] ([P, T/P, ...]) = rank-local reorder of srcs[t] ([T, ...])."""
     srcs, dsts = list(srcs), list(dsts)
-    if len(srcs) != len(dsts):
-        raise ValueError("srcs and dsts differ in length")
+    _check_gather(plan, srcs, dsts, plan.total_tokens, plan.padded_tokens, _row_elems(srcs[0]) if srcs else 0)
     _check(_lib.cpt_partition(plan.handle, len(srcs), ctypes.cast(_ptr_array(srcs), _vp),
                               ctypes.cast(_ptr_array(dsts), _vp), _row_elems(srcs[0]), _dtype_code(srcs[0]),
                               _stream(stream)))
@@ -324,8 +378,7 @@ def cpt_partition(plan: Plan, srcs, dsts, stream=None):
 def cpt_partition_rows(plan: Plan, srcs, dsts, local_begin: int, local_count: int, stream=None):
     """cpt_partition for flattened local rows [local_begin, local_begin + local_count) only."""
     srcs, dsts = list(srcs), list(dsts)
-    if len(srcs) != len(dsts):
-        raise ValueError("srcs and dsts differ in length")
+    _check_gather(plan, srcs, dsts, plan.total_tokens, plan.padded_tokens, _row_elems(srcs[0]) if srcs else 0)
     _check(_lib.cpt_partition_rows(plan.handle, len(srcs), ctypes.cast(_ptr_array(srcs), _vp),
                                    ctypes.cast(_ptr_array(dsts), _vp), _row_elems(srcs[0]),
                                    _dtype_code(srcs[0]), local_begin, local_count, _stream(stream)))
@@ -334,11 +387,25 @@ def cpt_partition_rows(plan: Plan, srcs, dsts, local_begin: int, local_count: in
 def cpt_restore(plan: Plan, srcs, dsts, stream=None):
     """dsts[t] ([T, ...]) = global-order copy of the rank-local srcs[t] ([P, T/P, ...])."""
     srcs, dsts = list(srcs), list(dsts)
-    if len(srcs) != len(dsts):
-        raise ValueError("srcs and dsts differ in length")
+    _check_gather(plan, srcs, dsts, plan.padded_tokens, plan.total_tokens, _row_elems(dsts[0]) if dsts else 0)
     _check(_lib.cpt_restore(plan.handle, len(srcs), ctypes.cast(_ptr_array(srcs), _vp),
                             ctypes.cast(_ptr_array(dsts), _vp), _row_elems(dsts[0]),
                             _dtype_code(srcs[0]), _stream(stream)))
+
+
+def _check_gather(plan: Plan, srcs, dsts, src_rows: int, dst_rows: int, row: int):
+    """Partition, restore: as many sources as destinations, one dtype, every
+    buffer large enough for its rows of `row` elements."""
+    if len(srcs) != len(dsts):
+        raise ValueError("srcs and dsts differ in length")
+    if not srcs:
+        return
+    esz = srcs[0].element_size()
+    for i, (a, b) in enumerate(zip(srcs, dsts)):
+        if a.dtype != srcs[0].dtype or b.dtype != srcs[0].dtype:
+            raise ValueError("srcs and dsts must share one dtype")
+        _need(a, src_rows * row * esz, f"srcs[{i}]")
+        _need(b, dst_rows * row * esz, f"dsts[{i}]")
 
 
 def _row_elems(t: torch.Tensor) -> int:
@@ -349,12 +416,26 @@ def _row_elems(t: torch.Tensor) -> int:
     return n
 
 
+def _check_grad_return(Tpad: int, P: int, dkw, dvw, dko, dvo):
+    """Writers of Tpad rows, owners of Tpad / P rows, one row width; the dV
+    pair like the dK pair."""
+    row = dkw.row_elems()
+    _need_parts(dkw, Tpad, row, "dk_writers")
+    _need_parts(dko, Tpad // P, row, "dk_owners")
+    if dvw is not None and dvo is not None:  # one without the other: the library refuses it
+        if dvw.dtype != dkw.dtype or dvo.dtype != dko.dtype:
+            raise ValueError("the dV pair must have the dtypes of the dK pair")
+        _need_parts(dvw, Tpad, row, "dv_writers")
+        _need_parts(dvo, Tpad // P, row, "dv_owners")
+
+
 def _grad_return(fn, plan: Plan, dk_writers, dv_writers, dk_owners, dv_owners, stream):
     P = plan.cp_size
     dkw = _Parts(dk_writers, P)
     dko = _Parts(dk_owners, P)
     dvw = _Parts(dv_writers, P) if dv_writers is not None else None
     dvo = _Parts(dv_owners, P) if dv_owners is not None else None
+    _check_grad_return(plan.padded_tokens, P, dkw, dvw, dko, dvo)
     _check(fn(plan.handle, dkw.array(), dvw.array() if dvw is not None else None, dko.array(),
               dvo.array() if dvo is not None else None, dkw.row_elems(), dkw.code(), dko.code(),
               _stream(stream)))
@@ -377,6 +458,7 @@ def cpt_grad_return_rows(plan: Plan, dk_writers, dv_writers, dk_owners, dv_owner
     dko = _Parts(dk_owners, P)
     dvw = _Parts(dv_writers, P) if dv_writers is not None else None
     dvo = _Parts(dv_owners, P) if dv_owners is not None else None
+    _check_grad_return(plan.padded_tokens, P, dkw, dvw, dko, dvo)
     _check(_lib.cpt_grad_return_rows(
         plan.handle, dkw.array(), dvw.array() if dvw is not None else None, dko.array(),
         dvo.array() if dvo is not None else None, dkw.row_elems(), dkw.code(), dko.code(),
@@ -406,6 +488,10 @@ def cpt_grad_return_noalloc(layout: int, cp_size: int, cu_seqlens, total_tokens:
     dko = _Parts(dk_owners, P)
     dvw = _Parts(dv_writers, P) if dv_writers is not None else None
     dvo = _Parts(dv_owners, P) if dv_owners is not None else None
+    # batches the library refuses on size grounds never reach a kernel
+    Tmap = _padded_total(layout, P, list(arr)) if 1 <= P <= CPT_MAX_CP_SIZE else 0
+    if 0 < Tmap <= CPT_NOALLOC_MAX_TOKENS and n <= CPT_NOALLOC_MAX_DOCS:
+        _check_grad_return(Tmap, P, dkw, dvw, dko, dvo)
     _check(_lib.cpt_grad_return_noalloc(
         layout, P, ctypes.cast(arr, _vp), n, total_tokens, dkw.array(),
         dvw.array() if dvw is not None else None, dko.array(),
@@ -416,6 +502,11 @@ def cpt_grad_return_noalloc(layout: int, cp_size: int, cu_seqlens, total_tokens:
 def cpt_grad_scatter(plan: Plan, writer: int, src: torch.Tensor, slots, self_slot, stream=None):
     """slots[o] ([T/P, ...]) = writer's rows owned by o; self_slot must be slots[writer]."""
     sl = _Parts(slots, plan.cp_size)
+    row = _row_elems(src)
+    _need(src, plan.padded_tokens * row * src.element_size(), "src")
+    if sl.dtype != src.dtype:
+        raise ValueError("slots must have the dtype of src")
+    _need_parts(sl, plan.padded_tokens // plan.cp_size, row, "slots")
     _check(_lib.cpt_grad_scatter(plan.handle, writer, _ptr(src), sl.array(), _ptr(self_slot),
                                  _row_elems(src), _dtype_code(src), _stream(stream)))
 
@@ -426,6 +517,9 @@ def cpt_slot_reduce(slots, dst: torch.Tensor, status: torch.Tensor | int | None 
     numel = 1
     for d in sl.shape:
         numel *= int(d)
+    _need(dst, numel * dst.element_size(), "dst")
+    if isinstance(status, torch.Tensor):
+        _need(status, 4, "status", torch.int32)
     _check(_lib.cpt_slot_reduce(sl.array(), n, numel, sl.code(), _dtype_code(dst), _ptr(dst),
                                 _ptr(status), _stream(stream)))
 
@@ -491,8 +585,8 @@ def cpt_epoch_status(ep: Epoch, owner: int, stream=None) -> int:
 
 
 def cpt_set_kernel_path(kernel: int):
-    """Process-wide kernel choice of the fused gradient return:
-    CPT_KERNEL_AUTO (measured rule), _LOADS or _BULK."""
+    """Process-wide kernel choice of the row gather, the gradient return and
+    the slot reduce: CPT_KERNEL_AUTO (measured rule), _LOADS or _BULK."""
     _check(_lib.cpt_set_kernel_path(kernel))
 
 
