@@ -24,8 +24,10 @@
  *
  * Conventions that hold for every call:
  *   Memory      The caller owns every buffer. The library never allocates
- *               device memory; a plan lives in a caller-provided device
- *               workspace (the memory-management answer in "Kernel-level
+ *               device memory at call time; a plan lives in a caller-provided
+ *               device workspace (the only device memory of its own is the
+ *               fixed array of cpt_grad_return_noalloc, part of the loaded
+ *               module; the memory-management answer in "Kernel-level
  *               compute-communication overlapping for CP linear attention
  *               kernels via nvshmem", cuLA issue 15: buffers whose lifetime
  *               the caller controls; [TE-3235] "Description": peer tensor
@@ -375,7 +377,7 @@ CPT_API cpt_status cpt_grad_return_accumulate(const cpt_plan *plan, const void *
                                               void *stream);
 
 /* Choose the kernel of the HBM-bound calls, for the whole process and every
- * device (paper has no counterpart: a tuning and testing control of this
+ * device (the pages have no counterpart: a tuning and testing control of this
  * implementation). The choice covers the row gather (cpt_partition,
  * cpt_partition_rows, cpt_restore, cpt_grad_scatter), the fused gradient
  * return (cpt_grad_return, cpt_grad_return_rows, cpt_grad_return_noalloc)
@@ -417,7 +419,7 @@ typedef enum cpt_call {
 } cpt_call;
 
 /* Which kernel a call would run under the current cpt_set_kernel_path
- * setting, with the same decision the launchers make (paper has no
+ * setting, with the same decision the launchers make (the pages have no
  * counterpart). Host-only; touches no device.
  *  call        the call family.
  *  cp_size     P: writers for the gradient return, slots for the slot
@@ -554,7 +556,7 @@ CPT_API cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *st
 
 /* Count of bounded waits inside this library's kernels that ran out of
  * their budget on the current device, since the library was loaded or last
- * reset (paper has no counterpart: it is this implementation's failure
+ * reset (the pages have no counterpart: it is this implementation's failure
  * report). The bulk-copy kernels of the row gather, the gradient return and
  * the slot reduce move data through shared memory, each copy completing on
  * an mbarrier. Every wait on one gives up after about a second or 2^24 polls.
@@ -568,7 +570,7 @@ CPT_API cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *st
  *  Errors: CPT_ERR_INVALID_ARG (NULL count), CPT_ERR_DEVICE, CPT_ERR_CUDA. */
 CPT_API cpt_status cpt_kernel_wait_timeouts(uint32_t *count, int32_t reset);
 
-/* Test switch for the failure path of the bulk-copy kernels (paper has no
+/* Test switch for the failure path of the bulk-copy kernels (the pages have no
  * counterpart). While on, every bulk-copy mbarrier of later launches on the
  * current device announces 16 bytes more than its copies deliver. Every
  * copy still completes, and nothing faults, but each wait runs out of its
