@@ -230,6 +230,14 @@ def _nbytes(t: torch.Tensor) -> int:
     return t.numel() * t.element_size()
 
 
+_ELEM_BYTES = {torch.float32: 4, torch.bfloat16: 2, torch.int32: 4}
+
+
+def _elem_bytes(dtype) -> int:
+    n = _ELEM_BYTES.get(dtype)
+    return n if n is not None else torch.empty(0, dtype=dtype).element_size()
+
+
 def _need(t, nbytes: int, what: str, dtype=None):
     """Refuse a buffer smaller than the bytes the call will touch (the C ABI
     sees only its address), or of the wrong element type."""
@@ -247,7 +255,7 @@ def _need_parts(parts, rows: int, row_elems: int, what: str):
         return
     if parts.row_elems() != row_elems:
         raise ValueError(f"{what} rows have {parts.row_elems()} elements, expected {row_elems}")
-    need = rows * row_elems * torch.tensor([], dtype=parts.dtype).element_size()
+    need = rows * row_elems * _elem_bytes(parts.dtype)
     if parts.part_bytes < need:
         raise ValueError(f"each part of {what} holds {parts.part_bytes} bytes but the call touches {need}")
 
