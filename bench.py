@@ -947,7 +947,7 @@ def run_next_rows(args):
         del dkw, dvw, dko, dvo
         torch.cuda.empty_cache()
 
-    # the other grad_return shapes of the survey's configurations: the
+    # the other grad_return configurations: the
     # single-document case (S=32768, 8x128; its 0.67 GB are close to L2 size,
     # so each launch is preceded by a 512 MB write that flushes L2) and the
     # lognormal packed batch (T=131072, 16x128) under both layouts
