@@ -81,6 +81,8 @@ _sig("cpt_plan_create", ctypes.c_int, ctypes.c_int, _i32, _vp, _i32, _i64, _vp, 
 _sig("cpt_plan_destroy", ctypes.c_int, _vp)
 _sig("cpt_plan_info", ctypes.c_int, _vp, ctypes.POINTER(_i64), ctypes.POINTER(_i32), ctypes.POINTER(_i32))
 _sig("cpt_plan_padded_tokens", ctypes.c_int, _vp, ctypes.POINTER(_i64))
+_sig("cpt_layout_padded_tokens", ctypes.c_int, ctypes.c_int, _i32, _vp, _i32, _i64,
+     ctypes.POINTER(_i64))
 _sig("cpt_thd_real_lengths", ctypes.c_int, _vp, _vp, _vp)
 _sig("cpt_index_map", ctypes.c_int, _vp, _vp, _vp, _vp)
 _sig("cpt_thd_metadata", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
@@ -267,15 +269,6 @@ def _same_kind(ts, what: str):
             raise ValueError(f"the {what} tensors differ in dtype or row width")
 
 
-def _padded_total(layout: int, cp_size: int, cu_vals) -> int:
-    """Tokens after per-document padding to multiples of 2*cp_size (padded
-    layout), else the total."""
-    if layout != CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED:
-        return int(cu_vals[-1]) if len(cu_vals) else 0
-    m = 2 * cp_size
-    return sum((int(b) - int(a) + m - 1) // m * m for a, b in zip(cu_vals[:-1], cu_vals[1:]))
-
-
 def _cu_array(cu_seqlens):
     vals = [int(v) for v in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
     return (_i32 * len(vals))(*vals), len(vals) - 1
@@ -291,6 +284,17 @@ def cpt_validate_layout(layout: int, cp_size: int, cu_seqlens, total_tokens: int
 
 def cpt_plan_workspace_bytes(layout: int, cp_size: int, n_docs: int, total_tokens: int) -> int:
     return int(_lib.cpt_plan_workspace_bytes(layout, cp_size, n_docs, total_tokens))
+
+
+def cpt_layout_padded_tokens(layout: int, cp_size: int, cu_seqlens, total_tokens: int) -> int:
+    """Tokens of the buffer the layout partitions (the padded total for the
+    padded layout, else total_tokens); raises CptError for a batch the
+    layout rejects."""
+    arr, n = _cu_array(cu_seqlens)
+    v = _i64(0)
+    _check(_lib.cpt_layout_padded_tokens(layout, cp_size, ctypes.cast(arr, _vp), n, total_tokens,
+                                         ctypes.byref(v)))
+    return int(v.value)
 
 
 # ------------------------------------------------------------------ plan
@@ -496,10 +500,14 @@ def cpt_grad_return_noalloc(layout: int, cp_size: int, cu_seqlens, total_tokens:
     dko = _Parts(dk_owners, P)
     dvw = _Parts(dv_writers, P) if dv_writers is not None else None
     dvo = _Parts(dv_owners, P) if dv_owners is not None else None
-    # batches the library refuses on size grounds never reach a kernel
-    Tmap = _padded_total(layout, P, list(arr)) if 1 <= P <= CPT_MAX_CP_SIZE else 0
-    if 0 < Tmap <= CPT_NOALLOC_MAX_TOKENS and n <= CPT_NOALLOC_MAX_DOCS:
-        _check_grad_return(Tmap, P, dkw, dvw, dko, dvo)
+    # the library sizes the map; batches it refuses (on layout or size
+    # grounds) are left to the call itself to report
+    Tmap = _i64(0)
+    if _lib.cpt_layout_padded_tokens(layout, P, ctypes.cast(arr, _vp), n, total_tokens,
+                                     ctypes.byref(Tmap)) != CPT_OK:
+        Tmap.value = 0
+    if 0 < Tmap.value <= CPT_NOALLOC_MAX_TOKENS and n <= CPT_NOALLOC_MAX_DOCS:
+        _check_grad_return(Tmap.value, P, dkw, dvw, dko, dvo)
     _check(_lib.cpt_grad_return_noalloc(
         layout, P, ctypes.cast(arr, _vp), n, total_tokens, dkw.array(),
         dvw.array() if dvw is not None else None, dko.array(),

@@ -176,6 +176,17 @@ struct WsLayout {
 
 bool is_padded(cpt_layout layout) { return layout == CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED; }
 
+// A document of L tokens padded at its end to the next multiple of 2P.
+int64_t padded_len(int64_t L, int P) { return (L + 2 * P - 1) / (2 * P) * (2 * P); }
+
+// Sum of the padded lengths of every document.
+int64_t padded_sum(const int32_t *cu, int32_t n, int P)
+{
+    int64_t Tpad = 0;
+    for (int32_t i = 0; i < n; ++i) Tpad += padded_len((int64_t)cu[i + 1] - cu[i], P);
+    return Tpad;
+}
+
 // Largest padded token count for n documents of T tokens: each document
 // grows by at most 2P-1 padding tokens.
 int64_t padded_cap(cpt_layout layout, int P, int n, int64_t T)
@@ -324,11 +335,7 @@ cpt_status cpt_validate_layout(cpt_layout layout, int32_t P, const int32_t *cu, 
             return fail(CPT_ERR_INVALID_ARG, "cu_seqlens decreases at %d (%d -> %d)", i, cu[i],
                         cu[i + 1]);
     if (is_padded(layout)) {
-        int64_t Tpad = 0;
-        for (int32_t i = 0; i < n; ++i) {
-            const int64_t L = cu[i + 1] - cu[i];
-            Tpad += (L + 2 * P - 1) / (2 * P) * (2 * P);
-        }
+        const int64_t Tpad = padded_sum(cu, n, P);
         if (Tpad > 0x7FFFFFFF)
             return fail(CPT_ERR_INVALID_ARG, "padded total %lld exceeds 2^31 - 1", (long long)Tpad);
     } else if (layout == CPT_LAYOUT_DUAL_CHUNK_SWAP) {
@@ -350,6 +357,16 @@ size_t cpt_plan_workspace_bytes(cpt_layout layout, int32_t P, int32_t n, int64_t
 {
     if (check_sizes(layout, P, n, T) != CPT_OK) return 0;
     return ws_layout(layout, P, n, T).total;
+}
+
+cpt_status cpt_layout_padded_tokens(cpt_layout layout, int32_t P, const int32_t *cu, int32_t n,
+                                   int64_t T, int64_t *padded_total)
+{
+    if (padded_total == nullptr) return fail(CPT_ERR_INVALID_ARG, "padded_total is NULL");
+    cpt_status st = cpt_validate_layout(layout, P, cu, n, T);
+    if (st) return st;
+    *padded_total = is_padded(layout) ? padded_sum(cu, n, P) : T;
+    return CPT_OK;
 }
 
 cpt_status cpt_plan_create(cpt_layout layout, int32_t P, const int32_t *cu, int32_t n, int64_t T,
@@ -406,7 +423,7 @@ cpt_status cpt_plan_create(cpt_layout layout, int32_t P, const int32_t *cu, int3
         p->h_cup[0] = 0;
         for (int32_t i = 0; i < n; ++i) {
             const int32_t L = cu[i + 1] - cu[i];
-            p->h_cup[i + 1] = p->h_cup[i] + (L + 2 * P - 1) / (2 * P) * (2 * P);
+            p->h_cup[i + 1] = p->h_cup[i] + (int32_t)padded_len(L, P);
         }
         p->Tpad = p->h_cup[n];
         p->cup = reinterpret_cast<int32_t *>(base + w.cup);
@@ -1123,7 +1140,7 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
         cup[0] = 0;
         for (int32_t i = 0; i < n; ++i) {
             const int32_t L = cu[i + 1] - cu[i];
-            cup[i + 1] = cup[i] + (L + 2 * P - 1) / (2 * P) * (2 * P);
+            cup[i + 1] = cup[i] + (int32_t)padded_len(L, P);
         }
         cu_map = cup.data();
         Tmap = cup[n];
@@ -1131,9 +1148,10 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
     }
     if (Tmap > CPT_NOALLOC_MAX_TOKENS)
         return fail(CPT_ERR_INVALID_ARG,
-                    "total_tokens %lld exceeds the no-allocation limit of %d tokens "
+                    "%s %lld exceeds the no-allocation limit of %d tokens "
                     "(use cpt_plan_create with a workspace)",
-                    (long long)Tmap, CPT_NOALLOC_MAX_TOKENS);
+                    is_padded(layout) ? "padded total" : "total_tokens", (long long)Tmap,
+                    CPT_NOALLOC_MAX_TOKENS);
     if (n > CPT_NOALLOC_MAX_DOCS)
         return fail(CPT_ERR_INVALID_ARG,
                     "n_docs %d exceeds the no-allocation limit of %d documents "
@@ -1147,6 +1165,8 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
     if ((st = check_row(row_elems, in, out, &units))) return st;
     int dev = 0;
     if (!current_device(&dev)) return fail(CPT_ERR_CUDA, "cudaGetDevice failed");
+    // the upload below reads a host vector that dies with this call
+    if ((st = refuse_capture(stream, "cpt_grad_return_noalloc"))) return st;
     int32_t *scratch = nullptr;
     if ((st = noalloc_scratch(dev, &scratch))) return st;
     if (Tmap == 0) return CPT_OK;

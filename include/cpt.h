@@ -187,6 +187,22 @@ CPT_API cpt_status cpt_validate_layout(cpt_layout layout, int32_t cp_size, const
 CPT_API size_t cpt_plan_workspace_bytes(cpt_layout layout, int32_t cp_size, int32_t n_docs,
                                 int64_t total_tokens);
 
+/* Tokens of the buffer a layout partitions, before any plan exists: for
+ * DUAL_CHUNK_SWAP_PADDED every document is padded at its end to the next
+ * multiple of 2*cp_size and the result is the sum of the padded lengths;
+ * for the other layouts it is total_tokens. Local buffers then hold
+ * padded_total/cp_size rows per rank. The pages name padding only as what
+ * the packed-contiguous policy avoids ([TE-3221] "Why", "Scope and
+ * constraints"); where the padding sits is this library's reading.
+ *  Arguments as for cpt_validate_layout; padded_total receives the count.
+ *  Host only: touches no device. The result equals cpt_plan_padded_tokens of
+ *  a plan built from the same arguments.
+ *  Errors: those of cpt_validate_layout (padded_total is left unchanged);
+ *  CPT_ERR_INVALID_ARG for a NULL padded_total. */
+CPT_API cpt_status cpt_layout_padded_tokens(cpt_layout layout, int32_t cp_size,
+                                            const int32_t *cu_seqlens_host, int32_t n_docs,
+                                            int64_t total_tokens, int64_t *padded_total);
+
 /* ------------------------------------------------------------------ */
 /* Plan: ownership maps and metadata, built once per batch              */
 /* ------------------------------------------------------------------ */
@@ -454,20 +470,27 @@ CPT_API cpt_status cpt_kernel_path_of(cpt_call call, int32_t cp_size, cpt_dtype 
  * cpt_grad_return; the output is bit-identical to a plan-based call. The map
  * is built into a file-scope device array inside the library instead of a
  * workspace, so the call allocates nothing:
- *  - Limits: total_tokens <= CPT_NOALLOC_MAX_TOKENS and n_docs <=
- *    CPT_NOALLOC_MAX_DOCS; larger batches are rejected with
+ *  - Limits: the tokens the map covers, at most CPT_NOALLOC_MAX_TOKENS, and
+ *    n_docs <= CPT_NOALLOC_MAX_DOCS. The tokens are total_tokens, except for
+ *    DUAL_CHUNK_SWAP_PADDED, where they are the padded total
+ *    (cpt_layout_padded_tokens), so a padded batch can be refused although
+ *    its raw total is within the limit. Larger batches are rejected with
  *    CPT_ERR_INVALID_ARG and a message naming the limit. The array is
  *    (CPT_NOALLOC_MAX_DOCS + 64 + CPT_NOALLOC_MAX_TOKENS) int32, about 4.5 MB,
  *    and every GPU that loads the library holds it until the process exits.
  *  - The first call on a device looks the array's device address up with
  *    that device current (a one-time set-up that enqueues nothing); make that
  *    first call before any stream capture.
+ *  - Each call uploads cu_seqlens from a host copy that lives only for the
+ *    length of the call, so a call made while its stream is being captured
+ *    returns CPT_ERR_UNSUPPORTED and enqueues nothing.
  *  - Every call shares the one array and leaves its map there. Calls ordered
  *    on one stream are safe; calls that overlap on the GPU (two streams, or
  *    two threads, at once) race on it and may return wrong sums.
  *  - Nothing in the array needs to start at zero: each call rewrites every
  *    map entry it reads.
- *  Errors: those of cpt_validate_layout and cpt_grad_return. */
+ *  Errors: those of cpt_validate_layout and cpt_grad_return;
+ *  CPT_ERR_UNSUPPORTED inside stream capture. */
 CPT_API cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t cp_size,
                                            const int32_t *cu_seqlens_host, int32_t n_docs,
                                            int64_t total_tokens, const void *const *dk_writers,

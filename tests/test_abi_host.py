@@ -162,3 +162,27 @@ def test_kernel_path_choice_validated(cpt):
             cpt.cpt_set_kernel_path(bad)
     for k in (cpt.CPT_KERNEL_LOADS, cpt.CPT_KERNEL_BULK, cpt.CPT_KERNEL_AUTO):
         cpt.cpt_set_kernel_path(k)
+
+
+def test_layout_padded_tokens_agrees_with_oracle(cpt, oracle_lib):
+    """The host-only padded-size query equals the last boundary of the
+    oracle's padded cu_seqlens, and the raw total for the other layouts."""
+    PAD = cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED
+    rng = np.random.default_rng(77)
+    for _ in range(300):
+        P = int(rng.integers(1, 9))
+        n = int(rng.integers(0, 9))
+        lens = rng.integers(0, 40, size=n)
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        T = int(cu[-1])
+        assert cpt.cpt_layout_padded_tokens(PAD, P, cu, T) == int(oracle_lib.pad_cu(P, cu)[-1])
+        if T % P == 0:
+            assert cpt.cpt_layout_padded_tokens(cpt.CPT_LAYOUT_PACKED_CONTIGUOUS, P, cu, T) == T
+    assert cpt.cpt_layout_padded_tokens(0, 4, [0, 64, 128], 128) == 128
+    assert cpt.cpt_layout_padded_tokens(PAD, 4, [0, 1, 1, 10], 10) == 8 + 0 + 16
+    with pytest.raises(cpt.CptError) as ei:
+        cpt.cpt_layout_padded_tokens(0, 4, [0, 6], 6)
+    assert ei.value.status == cpt.CPT_ERR_NOT_DIVISIBLE
+    with pytest.raises(cpt.CptError) as ei:
+        cpt.cpt_layout_padded_tokens(PAD, 8, [0, 1, 2**31 - 8], 2**31 - 8)
+    assert ei.value.status == cpt.CPT_ERR_INVALID_ARG

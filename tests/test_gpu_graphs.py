@@ -57,6 +57,11 @@ def test_host_state_calls_refuse_capture(cpt, cuda_device):
     ep = cpt.cpt_epoch_create(P)
     cpt.cpt_epoch_advance(ep)
     ws = torch.empty(cpt.cpt_plan_workspace_bytes(0, P, 1, 16), dtype=torch.uint8, device="cuda")
+    w = torch.ones((P, 16, 8), dtype=torch.bfloat16, device="cuda")
+    o = torch.full((P, 8, 8), 3.0, dtype=torch.bfloat16, device="cuda")
+    cpt.cpt_grad_return_noalloc(0, P, cu, 16, w, None, o, None)  # one-time set-up, outside capture
+    torch.cuda.synchronize()
+    o.fill_(3.0)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
@@ -64,13 +69,17 @@ def test_host_state_calls_refuse_capture(cpt, cuda_device):
     with torch.cuda.graph(g, stream=side):
         for fn in (lambda: cpt.cpt_plan_create(0, P, cu, 16, workspace=ws),
                    lambda: cpt.cpt_epoch_publish(ep, 0),
-                   lambda: cpt.cpt_epoch_wait(ep, 0)):
+                   lambda: cpt.cpt_epoch_wait(ep, 0),
+                   lambda: cpt.cpt_grad_return_noalloc(0, P, cu, 16, w, None, o, None)):
             try:
                 fn()
             except cpt.CptError as e:
                 errors.append((e.status, str(e)))
-    assert [s for s, _ in errors] == [cpt.CPT_ERR_UNSUPPORTED] * 3
+    assert [s for s, _ in errors] == [cpt.CPT_ERR_UNSUPPORTED] * 4
     assert all("stream capture" in m for _, m in errors)
+    # the refused allocation-free call enqueued nothing
+    torch.cuda.synchronize()
+    assert bool((o == 3.0).all().item())
     # the epoch bookkeeping is untouched: still nothing published
     torch.cuda.synchronize()
     with pytest.raises(cpt.CptError) as ei:

@@ -110,3 +110,13 @@ def test_host_validation_agrees_with_oracle(cpt, oracle_lib, layout, P, steps, t
     if P > 8 and want != 1:
         code = cpt.CPT_ERR_INVALID_ARG  # the library caps cp_size at 8
     assert got == code, (lay, P, cu.tolist(), T, cpt.cpt_last_error_string())
+
+
+@settings(max_examples=200, deadline=None)
+@given(raw_batches())
+def test_layout_padded_tokens_equals_oracle_pad_cu(cpt, oracle_lib, batch):
+    P, lens = batch
+    cu = _cu(lens)
+    T = int(cu[-1])
+    got = cpt.cpt_layout_padded_tokens(cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED, P, cu, T)
+    assert got == int(oracle_lib.pad_cu(P, cu)[-1])

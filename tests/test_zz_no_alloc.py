@@ -94,6 +94,25 @@ def test_noalloc_rejects_batches_beyond_its_limit(cpt, cuda_device):
     assert bool((o == 3.0).all().item())
 
 
+def test_noalloc_limit_applies_to_the_padded_total(cpt, cuda_device):
+    # 40,000 documents of 17 tokens: 680,000 raw tokens, within the limit,
+    # but each pads to 32 at P=8, so the map would cover 1,280,000 tokens
+    P, n, L = 8, 40000, 17
+    PAD = cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP_PADDED
+    cu = list(range(0, n * L + 1, L))
+    T = cu[-1]
+    assert T <= cpt.CPT_NOALLOC_MAX_TOKENS
+    assert cpt.cpt_layout_padded_tokens(PAD, P, cu, T) == n * 32 > cpt.CPT_NOALLOC_MAX_TOKENS
+    w = torch.empty((P, 1, 8), dtype=torch.bfloat16, device="cuda")
+    o = torch.full((P, 1, 8), 3.0, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cpt.CptError) as ei:
+        cpt.cpt_grad_return_noalloc(PAD, P, cu, T, w, None, o, None)
+    assert ei.value.status == cpt.CPT_ERR_INVALID_ARG
+    assert "padded total 1280000" in str(ei.value)
+    torch.cuda.synchronize()
+    assert bool((o == 3.0).all().item())
+
+
 def test_noalloc_padded_layout_matches_plan_path(cpt, cuda_device):
     P, lens = 4, [13, 0, 1000, 7]
     cu = synth.cu_from_lengths(lens)
