@@ -133,7 +133,8 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic(kernel: str, units: int):
-    """DRAM bytes per launch scaled from the committed ncu summary, or None
+    """(DRAM bytes per launch, how they were obtained), scaled from the
+    committed ncu summary by the units the launch processes; (None, reason)
     when the summary is missing or was taken on a different kernel source."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
     try:
@@ -144,10 +145,14 @@ def profiled_traffic(kernel: str, units: int):
                     k, v = line.split("=", 1)
                     kv[k.strip()] = v.strip()
         if kv.get("source_hash") != kernel_source_hash():
-            return None
-        return int(float(kv["dram_bytes_per_unit"]) * units)
+            return None, "kernel source changed since the ncu capture"
+        per_unit = float(kv["dram_bytes_per_unit"])
+        note = (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch at "
+                f"{kv.get('captured_at', 'the recorded case')}, {per_unit:.1f} B per {kv.get('unit', 'unit')}, "
+                f"x {units} units")
+        return int(per_unit * units), note
     except (OSError, KeyError, ValueError):
-        return None
+        return None, "no ncu record"
 
 
 # ---------------------------------------------------------------- ranks
@@ -445,6 +450,227 @@ def copy_ceiling_gbs(dev, stream) -> float:
     return 2 * (1 << 30) * 2 / (best / 1e3) / 1e9
 
 
+def _events_ms(fn, stream, reps, warm, before=None):
+    """Median CUDA-event time of fn() on `stream` over `reps` launches after
+    `warm`; `before` (e.g. an L2 flush) runs outside each timed interval."""
+    import torch
+
+    for _ in range(warm):
+        if before is not None:
+            before()
+        fn()
+    evs = []
+    for _ in range(reps):
+        if before is not None:
+            before()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+# Shapes tried for each mix ceiling: (block bytes, stages, CTAs per SM).
+CEILING_SHAPES = {
+    "read4_write1": [(10240, 4, 1), (8192, 4, 1), (12288, 4, 1), (5120, 4, 2), (5120, 8, 1), (16384, 3, 1)],
+    "read1_write1": [(32768, 4, 1), (40960, 4, 1), (16384, 4, 2), (8192, 4, 2), (32768, 3, 1), (24576, 8, 1)],
+}
+
+
+def mix_ceilings(cpt, srcs4, dst4, src1, dst1, stream, reps=10, warm=3):
+    """The fastest of a few bulk-copy shapes that move each call's read/write
+    mix with no arithmetic (cpt_stream_ceiling): 4 reads : 1 write (the
+    gradient return at P=4) and 1 : 1 (the row gather). GB/s counts read +
+    written bytes, like the kernels' algorithmic bytes."""
+    out = {}
+    for name, srcs, dst in (("read4_write1", srcs4, dst4), ("read1_write1", [src1], dst1)):
+        nbytes = dst.numel() * dst.element_size()
+        moved = (len(srcs) + 1) * nbytes
+        tried = []
+        for blk, stages, ctas in CEILING_SHAPES[name]:
+            ms = _events_ms(lambda: cpt.cpt_stream_ceiling(srcs, dst, blk, stages, ctas), stream, reps, warm)
+            tried.append((moved / (ms / 1e3) / 1e9, ms, blk, stages, ctas))
+        best = max(tried)
+        out[name] = {"gbs": best[0], "ms": best[1], "bytes": moved,
+                     "shape": {"block_bytes": best[2], "stages": best[3], "ctas_per_sm": best[4]},
+                     "tried_gbs": [round(t[0], 1) for t in tried]}
+    return out
+
+
+def staged_grad_return(cpt, plan, ep, dkw, dvw, dko, dvo, slots_k, slots_v, wstreams, ostreams, stream):
+    """The staged flow on 2P streams: P writer streams scatter their global
+    dK/dV into owner-major slots [owner][writer] and publish the epoch; P
+    owner streams wait for all writers and reduce their P slots in writer
+    order. The main stream waits for all of them."""
+    import torch
+
+    Pn = len(wstreams)
+    cpt.cpt_epoch_advance(ep)
+    start = torch.cuda.Event()
+    start.record(stream)
+    for w in range(Pn):
+        ws_ = wstreams[w]
+        ws_.wait_event(start)
+        cpt.cpt_grad_scatter(plan, w, dkw[w], [slots_k[o, w] for o in range(Pn)], slots_k[w, w], stream=ws_)
+        cpt.cpt_grad_scatter(plan, w, dvw[w], [slots_v[o, w] for o in range(Pn)], slots_v[w, w], stream=ws_)
+        cpt.cpt_epoch_publish(ep, w, stream=ws_)
+    for o in range(Pn):
+        os_ = ostreams[o]
+        os_.wait_event(start)
+        cpt.cpt_epoch_wait(ep, o, 1_000_000_000, cpt.CPT_WAIT_BOUNDED, stream=os_)
+        cpt.cpt_slot_reduce(slots_k[o], dko[o], ep.status_ptr(o), stream=os_)
+        cpt.cpt_slot_reduce(slots_v[o], dvo[o], ep.status_ptr(o), stream=os_)
+    for st in wstreams + ostreams:
+        stream.wait_stream(st)
+
+
+CONFIG_ROWS = ("single_doc", "lognormal_partition", "lognormal_grad_return", "slot_reduce", "pages_extras")
+
+
+def run_config_rows(cpt, synth, stream, dev, peak, names, reps=20, warm=3, big=None):
+    """Every configuration of the workload table besides the headline step,
+    timed with CUDA events on `stream` in this run. Each row gives time,
+    algorithmic bytes, GB/s, the fraction of the HBM peak and the kernel the
+    measured rule picked. `big` holds the pages-shaped step's tensors for the
+    restore, accumulate, allocation-free and staged rows."""
+    import torch
+
+    out = {}
+    BF = cpt.CPT_BF16
+
+    def kernel_of(call, Pk, in_dt, out_dt, acc, row_b, rows):
+        k = cpt.cpt_kernel_path_of(call, Pk, in_dt, out_dt, acc, row_b, rows)
+        return "bulk" if k == cpt.CPT_KERNEL_BULK else "loads"
+
+    def row(ms, nbytes, **extra):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        return {"ms": ms, "bytes": nbytes, "gbs": gbs, "frac_of_peak": gbs / peak, **extra}
+
+    if "single_doc" in names:
+        # P=4, S=32768 one document, 8x128 bf16 N(0,1): 0.67 GB per launch,
+        # close to the 129 MB L2 in reach, so a 512 MB write flushes L2 first
+        Tg, Hg = 32768, 8
+        rb = Hg * D * 2
+        plan = cpt.cpt_plan_create(0, P, [0, Tg], Tg)
+        wk = synth.device_normal_bf16((P, Tg, Hg, D), 7001, 1.0, dev)
+        wv = synth.device_normal_bf16((P, Tg, Hg, D), 7002, 1.0, dev)
+        ok = torch.empty((P, Tg // P, Hg, D), dtype=torch.bfloat16, device=dev)
+        ov = torch.empty_like(ok)
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        ms = _events_ms(lambda: cpt.cpt_grad_return(plan, wk, wv, ok, ov), stream, reps, warm,
+                        before=flush.zero_)
+        out["single_doc_grad_return_P4_S32768_8x128"] = row(
+            ms, Tg * (2 * (P + 1) * rb + 2 * 4), l2="flushed before each launch",
+            kernel=kernel_of(cpt.CPT_CALL_GRAD_RETURN, P, BF, BF, 0, rb, 2 * Tg))
+        del wk, wv, ok, ov, flush, plan
+
+    if "lognormal_partition" in names or "lognormal_grad_return" in names:
+        # T=131072 from lognormal document lengths, 16x128 bf16: per-document
+        # DualChunkSwap on lengths rounded to multiples of 8, packed-contiguous
+        # on the raw lengths; the Q/K/V partition and the dK+dV gradient return
+        Tl, Hl = 131072, 16
+        rb = Hl * D * 2
+        if "lognormal_partition" in names:
+            qkv = [synth.device_normal_bf16((Tl, Hl, D), 7100 + t, 1.0, dev) for t in range(3)]
+            loc = [torch.empty((P, Tl // P, Hl, D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+        if "lognormal_grad_return" in names:
+            wk = synth.device_normal_bf16((P, Tl, Hl, D), 7110, 1.0, dev)
+            wv = synth.device_normal_bf16((P, Tl, Hl, D), 7111, 1.0, dev)
+            ok = torch.empty((P, Tl // P, Hl, D), dtype=torch.bfloat16, device=dev)
+            ov = torch.empty_like(ok)
+        for name, layout, mult in (("per_document_dual_chunk_swap", 0, 8), ("packed_contiguous", 1, 1)):
+            lens = synth.lognormal_doc_lengths(Tl, synth.rng_for(2, 0), multiple=mult)
+            plan = cpt.cpt_plan_create(layout, P, synth.cu_from_lengths(lens), Tl)
+            if "lognormal_partition" in names:
+                ms = _events_ms(lambda: cpt.cpt_partition(plan, qkv, loc), stream, reps, warm)
+                out[f"lognormal_T131072_16x128_partition_{name}"] = row(
+                    ms, Tl * (3 * 2 * rb + 3 * 4), tok_s=Tl / (ms / 1e3), docs=len(lens),
+                    kernel="bulk" if cpt.cpt_kernel_path_of(cpt.CPT_CALL_ROW_GATHER, P, BF, BF, 0, rb,
+                                                            3 * Tl) == cpt.CPT_KERNEL_BULK else "loads")
+            if "lognormal_grad_return" in names:
+                ms = _events_ms(lambda: cpt.cpt_grad_return(plan, wk, wv, ok, ov), stream, reps, warm)
+                out[f"lognormal_T131072_16x128_grad_return_{name}"] = row(
+                    ms, Tl * (2 * (P + 1) * rb + 2 * 4), docs=len(lens),
+                    kernel=kernel_of(cpt.CPT_CALL_GRAD_RETURN, P, BF, BF, 0, rb, 2 * Tl))
+            del plan
+        if "lognormal_partition" in names:
+            del qkv, loc
+        if "lognormal_grad_return" in names:
+            del wk, wv, ok, ov
+
+    if "slot_reduce" in names:
+        # 8 slots, uniform[-1,1]: 1 KB and 1 MB per slot as latency (launched
+        # back to back from Python, and as replays of a graph of such calls),
+        # 1 GB per slot as bandwidth over 9 GB read + written
+        n_slots = 8
+        for dtype, tag, code in ((torch.float32, "f32", cpt.CPT_F32), (torch.bfloat16, "bf16", BF)):
+            esz = 4 if dtype == torch.float32 else 2
+            for label, nbytes in (("1KB", 1 << 10), ("1MB", 1 << 20), ("1GB", 1 << 30)):
+                n = nbytes // esz
+                gen = torch.Generator(device=dev)
+                gen.manual_seed(7200 + esz)
+                slots = [(torch.rand(n, device=dev, generator=gen) * 2 - 1).to(dtype) for _ in range(n_slots)]
+                dst = torch.empty(n, dtype=dtype, device=dev)
+                kern = kernel_of(cpt.CPT_CALL_SLOT_REDUCE, n_slots, code, code, 0, nbytes, 0)
+                if nbytes >= 1 << 30:
+                    ms = _events_ms(lambda: cpt.cpt_slot_reduce(slots, dst), stream, 10, warm)
+                    out[f"slot_reduce_8x{label}_{tag}"] = row(ms, (n_slots + 1) * nbytes, kernel=kern)
+                else:
+                    iters = 200
+                    launched = _events_ms(lambda: [cpt.cpt_slot_reduce(slots, dst) for _ in range(iters)],
+                                          stream, 3, 1) * 1e3 / iters
+                    side = torch.cuda.Stream(device=dev)
+                    side.wait_stream(stream)
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=side, capture_error_mode="relaxed"):
+                        for _ in range(iters):
+                            cpt.cpt_slot_reduce(slots, dst, stream=side)
+                    stream.wait_stream(side)
+                    graph_us = _events_ms(g.replay, stream, 3, 1) * 1e3 / iters
+                    out[f"slot_reduce_8x{label}_{tag}"] = {
+                        "us_per_call_launched": launched, "us_per_call_graph": graph_us,
+                        "bytes": (n_slots + 1) * nbytes, "kernel": kern,
+                        "note": "latency: L2-resident, back-to-back calls"}
+                    del g
+                del slots, dst
+
+    if "pages_extras" in names and big is not None:
+        # the widened rows at the pages' shape, on the step's own tensors
+        plan, qkv, part, dkw, dvw, dko, dvo = big
+        rb = H * D * 2
+        back = [torch.empty((S, H, D), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        ms = _events_ms(lambda: cpt.cpt_restore(plan, part[1:], back), stream, reps, warm)
+        out["pages_restore_kv"] = row(ms, S * (2 * 2 * rb + 2 * 4), tok_s=S / (ms / 1e3),
+                                      kernel="bulk" if cpt.cpt_kernel_path_of(
+                                          cpt.CPT_CALL_ROW_GATHER, P, BF, BF, 0, rb, 2 * S)
+                                      == cpt.CPT_KERNEL_BULK else "loads")
+        del back
+        ms = _events_ms(lambda: cpt.cpt_grad_return_accumulate(plan, dkw, dvw, dko, dvo), stream, reps, warm)
+        out["pages_grad_return_accumulate"] = row(ms, S * (2 * (P + 2) * rb + 2 * 4),
+                                                  kernel=kernel_of(cpt.CPT_CALL_GRAD_RETURN, P, BF, BF, 1,
+                                                                   rb, 2 * S))
+        ms = _events_ms(lambda: cpt.cpt_grad_return_noalloc(0, P, [0, S], S, dkw, dvw, dko, dvo), stream,
+                        reps, warm)
+        out["pages_grad_return_noalloc"] = row(ms, S * (2 * (P + 1) * rb + 2 * 4) + S * 4,
+                                               kernel=kernel_of(cpt.CPT_CALL_GRAD_RETURN, P, BF, BF, 0,
+                                                                rb, 2 * S),
+                                               note="includes its own map build each call")
+        slots_k = torch.empty((P, P, S // P, H, D), dtype=torch.bfloat16, device=dev)
+        slots_v = torch.empty_like(slots_k)
+        ep = cpt.cpt_epoch_create(P)
+        wst = [torch.cuda.Stream(device=dev) for _ in range(P)]
+        ost = [torch.cuda.Stream(device=dev) for _ in range(P)]
+        ms = _events_ms(lambda: staged_grad_return(cpt, plan, ep, dkw, dvw, dko, dvo, slots_k, slots_v,
+                                                   wst, ost, stream), stream, 10, warm)
+        out["pages_grad_return_staged"] = row(ms, S * 2 * ((3 * P + 1) * rb + P * 4), streams=2 * P,
+                                              note="scatter + publish + bounded wait + slot reduce")
+        del slots_k, slots_v
+    torch.cuda.synchronize()
+    return out
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -503,9 +729,6 @@ def run_gpu(args):
         cpt.cpt_plan_destroy(plan)
 
     if args.path == "staged":
-        # P writer streams scatter their global dK/dV into owner-major slots
-        # [owner][writer] and publish the epoch; P owner streams wait for all
-        # writers and reduce their P slots in writer order.
         slots_k = torch.empty((P, P, S // P, H, D), dtype=torch.bfloat16, device=dev)
         slots_v = torch.empty_like(slots_k)
         ep = cpt.cpt_epoch_create(P)
@@ -514,25 +737,7 @@ def run_gpu(args):
         kernels_per_step = 2 + 1 + P * 2 + P * 3  # plan, partition, scatters, checks + reduces
 
     def grad_return_staged(plan):
-        cpt.cpt_epoch_advance(ep)
-        start = torch.cuda.Event()
-        start.record(stream)
-        for w in range(P):
-            ws_ = wstreams[w]
-            ws_.wait_event(start)
-            cpt.cpt_grad_scatter(plan, w, dkw[w], [slots_k[o, w] for o in range(P)], slots_k[w, w],
-                                 stream=ws_)
-            cpt.cpt_grad_scatter(plan, w, dvw[w], [slots_v[o, w] for o in range(P)], slots_v[w, w],
-                                 stream=ws_)
-            cpt.cpt_epoch_publish(ep, w, stream=ws_)
-        for o in range(P):
-            os_ = ostreams[o]
-            os_.wait_event(start)
-            cpt.cpt_epoch_wait(ep, o, 1_000_000_000, cpt.CPT_WAIT_BOUNDED, stream=os_)
-            cpt.cpt_slot_reduce(slots_k[o], dko[o], ep.status_ptr(o), stream=os_)
-            cpt.cpt_slot_reduce(slots_v[o], dvo[o], ep.status_ptr(o), stream=os_)
-        for st in wstreams + ostreams:
-            stream.wait_stream(st)
+        staged_grad_return(cpt, plan, ep, dkw, dvw, dko, dvo, slots_k, slots_v, wstreams, ostreams, stream)
 
     gpu_uuid = None
     try:
@@ -689,6 +894,42 @@ def run_gpu(args):
             stream.wait_stream(h2d_stream)
             stream.wait_stream(d2h_stream)
 
+        # The host link's floor for one step, measured on the step's own
+        # pinned buffers before the e2e leg: every input copied in alone,
+        # every output copied out alone, and both at once on two streams.
+        dev_in, dev_out = qkv + [dkw, dvw], part + [dko, dvo]
+
+        def copies(inp, outp):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            h2d_stream.wait_stream(stream)
+            d2h_stream.wait_stream(stream)
+            if inp:
+                with torch.cuda.stream(h2d_stream):
+                    for d, h in zip(dev_in, host_in):
+                        d.copy_(h, non_blocking=True)
+            if outp:
+                with torch.cuda.stream(d2h_stream):
+                    for h, d in zip(host_out, dev_out):
+                        h.copy_(d, non_blocking=True)
+            stream.wait_stream(h2d_stream)
+            stream.wait_stream(d2h_stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b)
+
+        link = {}
+        for key, inp, outp in (("h2d_ms", True, False), ("d2h_ms", False, True), ("both_ms", True, True)):
+            copies(inp, outp)
+            link[key] = min(copies(inp, outp) for _ in range(2))
+        r_in = h2d / (link["h2d_ms"] / 1e3)
+        r_out = d2h / (link["d2h_ms"] / 1e3)
+        r_both = (h2d + d2h) / (link["both_ms"] / 1e3)
+        # even share: while both directions run, each gets half of the
+        # combined rate; the larger direction then finishes alone
+        lo, hi, r_hi = (d2h, h2d, r_in) if d2h <= h2d else (h2d, d2h, r_out)
+        link_floor_ms = (lo / (r_both / 2) + (hi - lo) / r_hi) * 1e3
+
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
         for i in range(2):  # warm-up: one step on each buffer set
             e2e_step(i)
@@ -718,7 +959,15 @@ def run_gpu(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": e2e_steps,
                "pipeline": (f"copies in, kernels, copies out on 3 streams over {len(pieces)} pieces, "
-                            "two buffer sets so consecutive steps overlap")}
+                            "two buffer sets so consecutive steps overlap"),
+               "link_floor_ms": link_floor_ms,
+               "vs_link_floor": e2e_ms / link_floor_ms,
+               "link": {"h2d_gbs": r_in / 1e9, "d2h_gbs": r_out / 1e9, "both_total_gbs": r_both / 1e9,
+                        "copies_only_ms": link["both_ms"],
+                        "how": ("the step's own pinned buffers copied in alone, out alone and both at "
+                                "once (best of 2, CUDA events) just before the e2e leg; floor = "
+                                "smaller direction at half the combined rate, then the rest of the "
+                                "larger direction alone")}}
         del host_in, host_out
 
     if rank != 0:
@@ -728,6 +977,25 @@ def run_gpu(args):
         return 0
 
     peak, peak_src = load_peak()
+    # mix-matched ceilings, into scratch buffers (the step's outputs stay as
+    # they are): P of the writer tensors -> one owner-sized buffer, and Q ->
+    # one local-sized buffer
+    scratch4 = torch.empty_like(dko)
+    scratch1 = torch.empty_like(part[0])
+    ceil = mix_ceilings(cpt, [dkw[w] for w in range(P)], scratch4, qkv[0], scratch1, stream)
+    del scratch4, scratch1
+    configs = {}
+    if args.configs != "none":
+        names = CONFIG_ROWS if args.configs == "all" else tuple(args.configs.split(","))
+        if (S, H) != (262144, 20):
+            names = tuple(n for n in names if n != "pages_extras")
+        plan_big = cpt.cpt_plan_create(cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP, P, cu, S, workspace=ws)
+        configs = run_config_rows(cpt, synth, stream, dev, peak, names, reps=args.config_reps,
+                                  warm=args.config_warmup,
+                                  big=(plan_big, qkv, part, dkw, dvw, dko, dvo))
+        cpt.cpt_plan_destroy(plan_big)
+    timeouts = cpt.cpt_kernel_wait_timeouts()
+    traffic, traffic_note = profiled_traffic("grad_return", S)
     gr_bytes = S * gr_bytes_per_token()
     gr_mean_ms = statistics.mean(gr_ms)
     gr_gbs = gr_bytes / (gr_mean_ms / 1e3) / 1e9
@@ -750,11 +1018,20 @@ def run_gpu(args):
         "grad_return": {"gbs": gr_gbs, "frac_of_peak": gr_gbs / peak, "ms": gr_mean_ms,
                         "bytes_per_launch": gr_bytes},
         "partition": {"tok_s": S / (part_mean_ms / 1e3), "gbs": part_gbs,
-                      "frac_of_peak": part_gbs / peak, "ms": part_mean_ms},
+                      "frac_of_peak": part_gbs / peak, "ms": part_mean_ms,
+                      "frac_mix": part_gbs / ceil["read1_write1"]["gbs"]},
         "roofline": {"kernel": "grad_return", "bound": "hbm", "achieved": gr_gbs, "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6800 GB/s", "unit": "GB/s", "frac": gr_gbs / peak,
-                     "traffic": profiled_traffic("grad_return", S) if PATH == "fused" else None},
+                     "frac_mix": gr_gbs / ceil["read4_write1"]["gbs"],
+                     "peak_mix": ceil["read4_write1"]["gbs"],
+                     "traffic": traffic if PATH == "fused" else None,
+                     "traffic_source": traffic_note if PATH == "fused" else None},
+        "ceilings": {**ceil, "how": ("cpt_stream_ceiling: the read/write mix of the call with no "
+                                     "arithmetic, bulk copies through shared memory; the fastest of "
+                                     "the shapes tried, CUDA events, median of 10 after 3")},
+        "configs": configs,
+        "wait_timeouts": timeouts,
         "copy_ceiling": {"gbs": copy_gbs, "grad_return_frac": gr_gbs / copy_gbs,
                          "partition_frac": part_gbs / copy_gbs,
                          "how": "torch copy_ of 1 Gi bf16 elements in this run, read+write bytes, "
@@ -1069,6 +1346,63 @@ def run_host_link_sweep(args):
     return 0
 
 
+def run_grad_return_size_sweep(args):
+    """The fused gradient return at P=4 with 2 KB rows (8x128 bf16, the
+    single-document configuration's rows) over launches of 0.17 to 5.4 GB,
+    each launch after an L2 flush (a 512 MB write), under the measured rule
+    and with each kernel forced. One JSON line per (kernel, size), then one
+    per kernel with a least-squares fit t = t0 + bytes / bw over the sizes,
+    which separates a fixed per-launch cost from the streaming rate."""
+    import torch
+
+    from context_attention_token_gb300 import build as cpt_build
+
+    cpt_build.build()
+    from context_attention_token_gb300 import cpt, synth
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    peak, peak_src = load_peak()
+    Hs = args.heads if args.heads != 20 else 8
+    rb = Hs * D * 2
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    sizes = (8192, 16384, 32768, 65536, 131072, 262144)
+    data = {name: [] for name in ("auto", "loads", "bulk")}
+    for Ts in sizes:
+        plan = cpt.cpt_plan_create(0, P, [0, Ts], Ts)
+        wk = synth.device_normal_bf16((P, Ts, Hs, D), 7301, 1.0, "cuda")
+        wv = synth.device_normal_bf16((P, Ts, Hs, D), 7302, 1.0, "cuda")
+        ok = torch.empty((P, Ts // P, Hs, D), dtype=torch.bfloat16, device="cuda")
+        ov = torch.empty_like(ok)
+        nbytes = Ts * (2 * (P + 1) * rb + 2 * 4)
+        for name, code in (("auto", cpt.CPT_KERNEL_AUTO), ("loads", cpt.CPT_KERNEL_LOADS),
+                           ("bulk", cpt.CPT_KERNEL_BULK)):
+            cpt.cpt_set_kernel_path(code)
+            ms = _events_ms(lambda: cpt.cpt_grad_return(plan, wk, wv, ok, ov), stream, 20, 3,
+                            before=flush.zero_)
+            data[name].append((nbytes, ms))
+            gbs = nbytes / (ms / 1e3) / 1e9
+            print(json.dumps({"sweep": "grad_return_launch_size", "kernel": name, "P": P, "S": Ts,
+                              "row_bytes": rb, "bytes": nbytes, "ms": ms, "gbs": gbs,
+                              "frac_of_peak": gbs / peak, "l2": "flushed before each launch"}), flush=True)
+        cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
+        del wk, wv, ok, ov, plan
+        torch.cuda.empty_cache()
+    for name, pts in data.items():
+        n = len(pts)
+        mx = sum(b for b, _ in pts) / n
+        my = sum(t for _, t in pts) / n
+        sxx = sum((b - mx) ** 2 for b, _ in pts)
+        slope = sum((b - mx) * (t - my) for b, t in pts) / sxx  # ms per byte
+        t0 = my - slope * mx
+        print(json.dumps({"sweep": "grad_return_launch_size_fit", "kernel": name, "t0_us": t0 * 1e3,
+                          "streaming_gbs": 1 / (slope / 1e3) / 1e9,
+                          "streaming_frac_of_peak": 1 / (slope / 1e3) / 1e9 / peak,
+                          "peak": peak, "peak_source": peak_src,
+                          "fit": "least squares of ms on bytes over all sizes"}), flush=True)
+    return 0
+
+
 def run_slot_reduce_sweep(args):
     """P slot buffers (--slots, default 8) of N bytes each, N = 1 KB x 4^k up to 1 GB, float32 and
     bf16: one ordered sum per launch. One JSON line per (dtype, N), with the
@@ -1186,13 +1520,18 @@ def main():
     ap.add_argument("--next-rows", action="store_true",
                     help="instead of the step: restore, accumulate, P sweep, no-alloc and "
                          "partition-policy lines")
-    ap.add_argument("--sweep", choices=["slot_reduce", "host_link"], default=None,
+    ap.add_argument("--sweep", choices=["slot_reduce", "host_link", "grad_return_sizes"], default=None,
                     help="instead of the step: the slot-reduce message-size sweep, or the "
                          "host link's copy rates")
     ap.add_argument("--kernel-path", choices=["auto", "loads", "bulk"], default="auto",
                     help="kernel of the gradient return and the slot reduce: the measured rule "
                          "(default), or one forced")
     ap.add_argument("--slots", type=int, default=8, help="--sweep slot_reduce: number of slots (1..8)")
+    ap.add_argument("--configs", default="all",
+                    help="configuration rows timed after the step: all, none, or a comma list of "
+                         + ", ".join(CONFIG_ROWS))
+    ap.add_argument("--config-reps", type=int, default=20, help="timed launches per configuration row")
+    ap.add_argument("--config-warmup", type=int, default=3, help="untimed launches per configuration row")
     ap.add_argument("--tokens", type=int, default=S, help="S (multiple of 2P)")
     ap.add_argument("--heads", type=int, default=H)
     args = ap.parse_args()
@@ -1209,6 +1548,8 @@ def main():
         return run_slot_reduce_sweep(args)
     if args.sweep == "host_link":
         return run_host_link_sweep(args)
+    if args.sweep == "grad_return_sizes":
+        return run_grad_return_size_sweep(args)
     if args.next_rows:
         return run_next_rows(args)
     return run_gpu(args)

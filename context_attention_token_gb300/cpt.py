@@ -10,6 +10,8 @@ function is registered with a GIL-release guard).
 
 The shared library must have been built (``context_attention_token_gb300.build``);
 importing this module without it raises ImportError: there is no fallback.
+With CPT_LIBRARY_VARIANT=checked in the environment the binding loads the
+bounds-checked build (libcpt_checked.so) instead of libcpt.so.
 """
 from __future__ import annotations
 
@@ -20,7 +22,10 @@ import re
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_PKG, "libcpt.so")
+_VARIANT = os.environ.get("CPT_LIBRARY_VARIANT", "release")
+if _VARIANT not in ("release", "checked"):
+    raise ImportError(f"CPT_LIBRARY_VARIANT={_VARIANT!r}: expected 'release' or 'checked'")
+_LIB_PATH = os.path.join(_PKG, "libcpt.so" if _VARIANT == "release" else "libcpt_checked.so")
 
 if not os.path.exists(_LIB_PATH):
     raise ImportError(
@@ -109,6 +114,9 @@ _sig("cpt_set_kernel_path", ctypes.c_int, _i32)
 _sig("cpt_test_stall_bulk_waits", ctypes.c_int, _i32)
 _sig("cpt_kernel_path_of", ctypes.c_int, _i32, _i32, _i32, _i32, _i32, _i64, _i64, ctypes.POINTER(_i32))
 _sig("cpt_slot_reduce", ctypes.c_int, _vp, _i32, _i64, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp)
+_sig("cpt_stream_ceiling", ctypes.c_int, _vp, _i32, _vp, _i64, _i32, _i32, _i32, _vp)
+_sig("cpt_bounds_checked", _i32)
+_sig("cpt_bounds_violations", ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), _i32)
 
 
 def library_path() -> str:
@@ -615,6 +623,18 @@ def cpt_kernel_path_of(call: int, cp_size: int, in_dtype: int, out_dtype: int, a
     return v.value
 
 
+def cpt_bounds_checked() -> bool:
+    """Whether the loaded library is the bounds-checked build."""
+    return bool(_lib.cpt_bounds_checked())
+
+
+def cpt_bounds_violations(reset: bool = False) -> int:
+    """Failed device bounds checks so far (bounds-checked build only)."""
+    v = ctypes.c_uint32(0)
+    _check(_lib.cpt_bounds_violations(ctypes.byref(v), 1 if reset else 0))
+    return int(v.value)
+
+
 def cpt_test_stall_bulk_waits(on: bool):
     """Test switch: make every bulk-copy wait of later launches run out of its
     budget (on) or behave normally (off)."""
@@ -628,6 +648,18 @@ def cpt_kernel_wait_timeouts(reset: bool = False) -> int:
     v = ctypes.c_uint32()
     _check(_lib.cpt_kernel_wait_timeouts(ctypes.byref(v), 1 if reset else 0))
     return v.value
+
+
+def cpt_stream_ceiling(srcs, dst: torch.Tensor, block_bytes: int, stages: int, ctas_per_sm: int = 1,
+                       stream=None):
+    """dst = copy of srcs[0], every other source read and discarded: the
+    read/write mix of an HBM-bound call with no arithmetic (a roofline
+    ceiling). All tensors hold the same number of bytes."""
+    sl = _Parts(srcs, len(srcs) if not isinstance(srcs, torch.Tensor) else srcs.shape[0])
+    nbytes = sl.part_bytes
+    _need(dst, nbytes, "dst")
+    _check(_lib.cpt_stream_ceiling(sl.array(), len(sl.ptrs), _ptr(dst), nbytes, block_bytes, stages,
+                                   ctas_per_sm, _stream(stream)))
 
 
 def declared_functions(header_path: str) -> list[str]:

@@ -608,6 +608,8 @@ static cpt_status partition_impl(const cpt_plan *plan, int32_t n_tensors, const 
     p.rows = (int64_t)n_tensors * count;
     p.units = (int32_t)units;
     p.row_bytes = (int32_t)row_bytes;
+    p.src_rows = plan->T;
+    p.parts = plan->P;
     cudaError_t e = launch_gather(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CPT_OK : cuda_fail(e, "partition launch");
 }
@@ -663,6 +665,7 @@ cpt_status cpt_restore(const cpt_plan *plan, int32_t n_tensors, const void *cons
             p.dst[t][0] = static_cast<uint8_t *>(dst[t]);
         }
         p.Tp = plan->T;
+        p.parts = 1;
     } else {
         // global row g of piece r (g = r*T/P + j) reads local row g2l[g]
         p.l2g = plan->layout == CPT_LAYOUT_PACKED_CONTIGUOUS ? nullptr : plan->g2l;
@@ -672,7 +675,9 @@ cpt_status cpt_restore(const cpt_plan *plan, int32_t n_tensors, const void *cons
                 p.dst[t][o] = static_cast<uint8_t *>(dst[t]) + (int64_t)o * plan->Tp * row_bytes;
         }
         p.Tp = plan->Tp;
+        p.parts = plan->P;
     }
+    p.src_rows = plan->Tpad;
     p.T = plan->T;
     p.rows = (int64_t)n_tensors * plan->T;
     p.units = (int32_t)units;
@@ -732,6 +737,7 @@ static cpt_status grad_return_impl(const cpt_plan *plan, const void *const *dkw,
     p.units = (int32_t)units;
     p.in_row_bytes = (int32_t)in_row;
     p.out_row_bytes = (int32_t)out_row;
+    p.w_rows = plan->Tpad;
     cudaError_t e =
         launch_grad_return(p, P, in, out, static_cast<cudaStream_t>(stream), accumulate);
     return e == cudaSuccess ? CPT_OK : cuda_fail(e, "grad_return launch");
@@ -805,6 +811,8 @@ cpt_status cpt_grad_scatter(const cpt_plan *plan, int32_t writer, const void *sr
     p.rows = plan->Tpad;
     p.units = (int32_t)units;
     p.row_bytes = (int32_t)row_bytes;
+    p.src_rows = plan->Tpad;
+    p.parts = P;
     cudaError_t e = launch_gather(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CPT_OK : cuda_fail(e, "grad_scatter launch");
 }
@@ -1070,13 +1078,74 @@ cpt_status cpt_kernel_wait_timeouts(uint32_t *count, int32_t reset)
     if (count == nullptr) return fail(CPT_ERR_INVALID_ARG, "NULL argument");
     int dev = 0;
     if (!current_device(&dev)) return fail(CPT_ERR_DEVICE, "no current CUDA device");
-    unsigned int v = 0, w = 0, x = 0;
+    unsigned int v = 0, w = 0, x = 0, y = 0;
     cudaError_t e = read_wait_timeouts(&v, reset != 0);
     if (e == cudaSuccess) e = read_slot_reduce_wait_timeouts(&w, reset != 0);
     if (e == cudaSuccess) e = read_gather_wait_timeouts(&x, reset != 0);
+    if (e == cudaSuccess) e = read_ceiling_wait_timeouts(&y, reset != 0);
     if (e != cudaSuccess) return cuda_fail(e, "wait-timeout counter read");
-    *count = v + w + x;
+    *count = v + w + x + y;
     return CPT_OK;
+}
+
+int32_t cpt_bounds_checked(void)
+{
+#ifdef CPT_CHECK_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+cpt_status cpt_bounds_violations(uint32_t *count, int32_t reset)
+{
+    Trace trace("cpt_bounds_violations");
+    if (count == nullptr) return fail(CPT_ERR_INVALID_ARG, "NULL argument");
+    if (!cpt_bounds_checked())
+        return fail(CPT_ERR_UNSUPPORTED, "this library was built without CPT_CHECK_BOUNDS");
+    int dev = 0;
+    if (!current_device(&dev)) return fail(CPT_ERR_DEVICE, "no current CUDA device");
+    unsigned int a = 0, b = 0, c = 0;
+    cudaError_t e = read_index_map_bounds_violations(&a, reset != 0);
+    if (e == cudaSuccess) e = read_gather_bounds_violations(&b, reset != 0);
+    if (e == cudaSuccess) e = read_grad_return_bounds_violations(&c, reset != 0);
+    if (e != cudaSuccess) return cuda_fail(e, "bounds counter read");
+    *count = a + b + c;
+    return CPT_OK;
+}
+
+cpt_status cpt_stream_ceiling(const void *const *srcs, int32_t n_src, void *dst, int64_t bytes,
+                              int32_t block_bytes, int32_t stages, int32_t ctas_per_sm, void *stream)
+{
+    Trace trace("cpt_stream_ceiling");
+    if (srcs == nullptr) return fail(CPT_ERR_INVALID_ARG, "srcs is NULL");
+    if (!ceiling_shape_ok(n_src, block_bytes, stages))
+        return fail(CPT_ERR_INVALID_ARG,
+                    "n_src %d, block_bytes %d, stages %d: need 1..8 sources, 2..8 stages, blocks of "
+                    "a multiple of 16 bytes and n_src * block_bytes * stages <= 200 KB",
+                    n_src, block_bytes, stages);
+    if (ctas_per_sm < 1 || ctas_per_sm > 32)
+        return fail(CPT_ERR_INVALID_ARG, "ctas_per_sm %d outside 1..32", ctas_per_sm);
+    if (bytes < 0 || bytes % 16 != 0)
+        return fail(CPT_ERR_ALIGNMENT, "bytes %lld is not a non-negative multiple of 16",
+                    (long long)bytes);
+    int dev = 0;
+    if (!current_device(&dev)) return fail(CPT_ERR_CUDA, "cudaGetDevice failed");
+    if (bytes == 0) return CPT_OK;
+    cpt_status st;
+    std::vector<Range> r;
+    const uint8_t *s8[CPT_MAX_CP_SIZE];
+    for (int k = 0; k < n_src; ++k) {
+        if ((st = check_ptr(srcs[k], dev, 16, "srcs", k))) return st;
+        add_range(r, srcs[k], (size_t)bytes, false, "srcs", k);
+        s8[k] = static_cast<const uint8_t *>(srcs[k]);
+    }
+    if ((st = check_ptr(dst, dev, 16, "dst"))) return st;
+    add_range(r, dst, (size_t)bytes, true, "dst");
+    if ((st = check_overlaps(r))) return st;
+    cudaError_t e = launch_stream_ceiling(s8, n_src, static_cast<uint8_t *>(dst), bytes, block_bytes,
+                                          stages, ctas_per_sm, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CPT_OK : cuda_fail(e, "stream ceiling launch");
 }
 
 }  // extern "C"
@@ -1225,6 +1294,7 @@ extern "C" cpt_status cpt_grad_return_noalloc(cpt_layout layout, int32_t P, cons
     p.units = (int32_t)units;
     p.in_row_bytes = (int32_t)in_row;
     p.out_row_bytes = (int32_t)out_row;
+    p.w_rows = Tmap;
     e = launch_grad_return(p, P, in, out, s);
     return e == cudaSuccess ? CPT_OK : cuda_fail(e, "grad_return launch");
 }

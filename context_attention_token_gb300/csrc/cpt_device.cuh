@@ -8,6 +8,51 @@
 
 namespace cpt {
 
+// ----------------------------------------------------------------- bounds checks
+//
+// Built with -DCPT_CHECK_BOUNDS, every index a kernel reads from memory (a
+// map entry, a document boundary) or derives from one (a rank, a local row)
+// is checked against the extent of the buffer it addresses before it is
+// used. A failed check adds one to this translation unit's device counter
+// and the access is skipped; nothing traps. Without the flag kCheckBounds is
+// false and the checks compile to nothing.
+#ifdef CPT_CHECK_BOUNDS
+constexpr bool kCheckBounds = true;
+static __device__ unsigned int g_bounds_violations;
+#else
+constexpr bool kCheckBounds = false;
+#endif
+
+// `ok`, counting a failure when `count` (one lane of a warp-wide check).
+__device__ __forceinline__ bool in_bounds(bool ok, bool count = true)
+{
+#ifdef CPT_CHECK_BOUNDS
+    if (!ok && count) atomicAdd(&g_bounds_violations, 1u);
+    return ok;
+#else
+    (void)ok;
+    (void)count;
+    return true;
+#endif
+}
+
+// This translation unit's failed-check count (0 without CPT_CHECK_BOUNDS).
+static inline cudaError_t read_bounds_counter(unsigned int *count, bool reset)
+{
+#ifdef CPT_CHECK_BOUNDS
+    cudaError_t e = cudaMemcpyFromSymbol(count, g_bounds_violations, sizeof(unsigned int));
+    if (e == cudaSuccess && reset) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_bounds_violations, &zero, sizeof(unsigned int));
+    }
+    return e;
+#else
+    (void)reset;
+    *count = 0;
+    return cudaSuccess;
+#endif
+}
+
 // 16-byte load of data read exactly once in this kernel: read-only path,
 // no L1 allocation.
 __device__ __forceinline__ uint4 ld_once(const void *p)

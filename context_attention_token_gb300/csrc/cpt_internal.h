@@ -51,6 +51,8 @@ struct GatherParams {
     int64_t rows;        // n_tensors * T
     int32_t units;       // 16-byte units per row
     int32_t row_bytes;
+    int64_t src_rows;    // rows of each source tensor (bounds checks)
+    int32_t parts;       // destination pieces per tensor (bounds checks)
 };
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream);
 
@@ -67,6 +69,7 @@ struct GradReturnParams {
     int32_t units;         // 16-byte input units per row
     int32_t in_row_bytes;
     int32_t out_row_bytes;
+    int64_t w_rows;        // rows of each writer tensor (bounds checks)
 };
 // Kernel of the row gather, the fused gradient return and the slot reduce:
 // 0 = the measured rule, 1 = 16-byte loads, 2 = bulk copies wherever they can
@@ -107,6 +110,20 @@ struct SlotReduceParams {
 };
 cudaError_t launch_slot_reduce(const SlotReduceParams &p, int n_slots, int in_dtype,
                                int out_dtype, cudaStream_t stream);
+
+// Streaming ceiling: dst = copy of srcs[0], srcs[1..n_src) read and
+// discarded, through the bulk-copy engine in blocks of block_bytes and a ring
+// of `stages` stages per CTA, at most ctas_per_sm CTAs per SM.
+bool ceiling_shape_ok(int n_src, int block_bytes, int stages);
+cudaError_t launch_stream_ceiling(const uint8_t *const *srcs, int n_src, uint8_t *dst, int64_t bytes,
+                                  int block_bytes, int stages, int ctas_per_sm, cudaStream_t stream);
+cudaError_t read_ceiling_wait_timeouts(unsigned int *count, bool reset);
+
+// Failed bounds checks of each translation unit's kernels since the last
+// reset (always 0 in a build without CPT_CHECK_BOUNDS). Synchronous.
+cudaError_t read_index_map_bounds_violations(unsigned int *count, bool reset);
+cudaError_t read_gather_bounds_violations(unsigned int *count, bool reset);
+cudaError_t read_grad_return_bounds_violations(unsigned int *count, bool reset);
 
 // Bounded epoch check: one warp polls flags_row[0..P) with acquire loads until
 // every (int32)(flag - epoch) >= 0, for at most timeout_ns, then writes 0 or

@@ -90,7 +90,13 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p)
         const int64_t q = p.q0 + (R - t * p.T);
         const int r = (int)(q / p.Tp);
         const int64_t j = q - (int64_t)r * p.Tp;
+        if constexpr (kCheckBounds) {
+            if (!in_bounds(q >= 0 && r < p.parts, lane == 0)) continue;
+        }
         const int64_t g = p.l2g ? (int64_t)__ldg(p.l2g + q) : q;
+        if constexpr (kCheckBounds) {
+            if (!in_bounds(g >= -1 && g < p.src_rows, lane == 0)) continue;
+        }
         uint8_t *dst = p.dst[t][r] + j * p.row_bytes;
         if (g < 0) {  // padding row of the padded layout
             for (int u = lane; u < units; u += 32) st_once(dst + (int64_t)u * 16, make_uint4(0, 0, 0, 0));
@@ -157,7 +163,12 @@ __global__ void __launch_bounds__(32) gather_blocks_kernel(const GatherParams p,
         const Blk b = block(i);
         if (lane >= b.n) return -2;
         const int64_t q = p.q0 + b.L0 + lane;
-        return p.l2g ? (int64_t)__ldg(p.l2g + q) : q;
+        int64_t g = p.l2g ? (int64_t)__ldg(p.l2g + q) : q;
+        // an entry outside the source is not read: its row is written as zeros
+        if constexpr (kCheckBounds) {
+            if (!in_bounds(g >= -1 && g < p.src_rows)) g = -1;
+        }
+        return g;
     };
     int64_t g_ahead = map_entry(0);
 
@@ -210,6 +221,9 @@ __global__ void __launch_bounds__(32) gather_blocks_kernel(const GatherParams p,
             const uint32_t q = (uint32_t)(p.q0 + b.L0 + j);
             const uint32_t r = q / Tp32;
             const uint32_t jj = q - r * Tp32;
+            if constexpr (kCheckBounds) {
+                if (!in_bounds(r < (uint32_t)p.parts)) break;
+            }
             const int len = (int)min((int64_t)(b.n - j), (int64_t)(Tp32 - jj));
             bulk_store(p.dst[b.t][r] + (int64_t)jj * rb, stage + (size_t)j * rb, (uint32_t)(len * rb));
             j += len;
@@ -298,6 +312,11 @@ bool gather_uses_blocks(int64_t row_bytes, int64_t rows)
     if (block_rows(row_bytes) == 0) return false;
     const int choice = kernel_path();
     return choice == 2 || (choice == 0 && prefer_blocks(row_bytes, rows));
+}
+
+cudaError_t read_gather_bounds_violations(unsigned int *count, bool reset)
+{
+    return read_bounds_counter(count, reset);
 }
 
 cudaError_t read_gather_wait_timeouts(unsigned int *count, bool reset)

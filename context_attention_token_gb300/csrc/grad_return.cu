@@ -185,7 +185,13 @@ __global__ void __launch_bounds__(kThreads) grad_return_kernel(const GradReturnP
         const int64_t q = p.q0 + (R - t * p.T);
         const int o = (int)(q / p.Tp);
         const int64_t j = q - (int64_t)o * p.Tp;
+        if constexpr (kCheckBounds) {
+            if (!in_bounds(q >= 0 && o < P, lane == 0)) continue;
+        }
         const int64_t g = __ldg(p.l2g + q);
+        if constexpr (kCheckBounds) {
+            if (!in_bounds(g >= 0 && g < p.w_rows, lane == 0)) continue;
+        }
         const uint8_t *src[P];
 #pragma unroll
         for (int w = 0; w < P; ++w) src[w] = (t ? p.w[1][w] : p.w[0][w]) + g * p.in_row_bytes;
@@ -286,7 +292,15 @@ __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const
     int64_t R = (int64_t)blockIdx.x * kBulkWarps + wid;
     int64_t g_next = 0;
     const uint32_t stall = g_stall_tx;
-    if (lane == 0 && R < p.rows) g_next = __ldg(p.l2g + p.q0 + (R >= p.T ? R - p.T : R));
+    // the map entry of local row q, or -1 (which fails the row's check) for a
+    // row outside the map in a bounds-checked build
+    auto map_at = [&](int64_t q) -> int64_t {
+        if constexpr (kCheckBounds) {
+            if (!in_bounds(q >= 0 && q < (int64_t)P * p.Tp)) return -1;
+        }
+        return __ldg(p.l2g + q);
+    };
+    if (lane == 0 && R < p.rows) g_next = map_at(p.q0 + (R >= p.T ? R - p.T : R));
     uint32_t phase = 0;
 
     for (; R < p.rows; R += stride) {
@@ -294,20 +308,27 @@ __global__ void __launch_bounds__(32 * kBulkWarps) grad_return_bulk_kernel(const
         const int64_t q = p.q0 + (R - t * p.T);
         const int o = (int)(q / p.Tp);
         const int64_t j = q - (int64_t)o * p.Tp;
+        bool row_ok = true;
         if (lane == 0) {
             const int64_t g = g_next;
-            // accumulate mode reloads `out` with the owner's current row: the
-            // previous row's store must have read it first
-            if constexpr (ACC) bulk_wait_read<0>();
-            mbar_expect_tx(bar, (uint32_t)(P * rb + (ACC ? ob : 0)) + stall);
+            if constexpr (kCheckBounds) row_ok = in_bounds(o < P && g >= 0 && g < p.w_rows);
+            if (row_ok) {
+                // accumulate mode reloads `out` with the owner's current row:
+                // the previous row's store must have read it first
+                if constexpr (ACC) bulk_wait_read<0>();
+                mbar_expect_tx(bar, (uint32_t)(P * rb + (ACC ? ob : 0)) + stall);
 #pragma unroll
-            for (int w = 0; w < P; ++w)
-                bulk_load(stage + (size_t)w * rb, (t ? p.w[1][w] : p.w[0][w]) + g * rb, (uint32_t)rb,
-                          bar);
-            if constexpr (ACC)
-                bulk_load(out, (t ? p.o[1][o] : p.o[0][o]) + j * ob, (uint32_t)ob, bar);
+                for (int w = 0; w < P; ++w)
+                    bulk_load(stage + (size_t)w * rb, (t ? p.w[1][w] : p.w[0][w]) + g * rb,
+                              (uint32_t)rb, bar);
+                if constexpr (ACC)
+                    bulk_load(out, (t ? p.o[1][o] : p.o[0][o]) + j * ob, (uint32_t)ob, bar);
+            }
             const int64_t Rn = R + stride;
-            if (Rn < p.rows) g_next = __ldg(p.l2g + p.q0 + (Rn >= p.T ? Rn - p.T : Rn));
+            if (Rn < p.rows) g_next = map_at(p.q0 + (Rn >= p.T ? Rn - p.T : Rn));
+        }
+        if constexpr (kCheckBounds) {
+            if (!__shfl_sync(0xFFFFFFFFu, row_ok, 0)) continue;  // a skipped row: nothing in flight
         }
         const bool ok = mbar_wait_bounded(bar, phase);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
@@ -477,6 +498,11 @@ cudaError_t read_wait_timeouts(unsigned int *count, bool reset)
         e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(unsigned int));
     }
     return e;
+}
+
+cudaError_t read_grad_return_bounds_violations(unsigned int *count, bool reset)
+{
+    return read_bounds_counter(count, reset);
 }
 
 cudaError_t launch_grad_return(const GradReturnParams &p, int cp_size, int in_dtype,

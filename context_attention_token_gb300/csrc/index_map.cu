@@ -10,6 +10,7 @@
 // The kernels here (the map, the metadata, the padded layout's extra maps
 // and the real-token counts) are integer-only and move a few bytes per token;
 // they are launch-bound at the sizes used here, so they favour simplicity.
+#include "cpt_device.cuh"
 #include "cpt_internal.h"
 
 namespace cpt {
@@ -37,12 +38,18 @@ __global__ void index_map_kernel(int layout, int P, const int32_t *__restrict__ 
                 const int mid = (lo + hi) >> 1;
                 if (__ldg(cu + mid) / P <= j) lo = mid; else hi = mid;
             }
+            if constexpr (kCheckBounds) {
+                if (!in_bounds(lo >= 0 && lo < n)) continue;
+            }
             const int64_t c0 = __ldg(cu + lo);
             const int64_t m = (__ldg(cu + lo + 1) - c0) / (2 * P);
             const int64_t u = j - c0 / P;
             g = (u < m) ? c0 + r * m + u : c0 + (2 * P - 1 - r) * m + (u - m);
         } else {
             g = q;
+        }
+        if constexpr (kCheckBounds) {
+            if (!in_bounds(g >= 0 && g < T)) continue;
         }
         l2g[q] = (int32_t)g;
         if (g2l) g2l[g] = (int32_t)q;
@@ -86,7 +93,8 @@ __global__ void thd_metadata_kernel(int layout, int P, const int32_t *__restrict
                     nonempty = lo < hi;
                 }
                 const unsigned ballot = __ballot_sync(0xFFFFFFFFu, nonempty);
-                if (nonempty) row[count + __popc(ballot & ((1u << lane) - 1u))] = (int32_t)(lo - a);
+                const int slot = count + __popc(ballot & ((1u << lane) - 1u));
+                if (nonempty && in_bounds(slot <= n)) row[slot] = (int32_t)(lo - a);
                 if (first < 0 && ballot) first = base + __ffs(ballot) - 1;
                 count += __popc(ballot);
             }
@@ -128,6 +136,9 @@ __global__ void pad_maps_kernel(const int32_t *__restrict__ cu, const int32_t *_
             const int mid = (lo + hi) >> 1;
             if (__ldg(cup + mid) <= gp) lo = mid; else hi = mid;
         }
+        if constexpr (kCheckBounds) {
+            if (!in_bounds(gp >= 0 && gp < Tpad && lo >= 0 && lo < n)) continue;
+        }
         const int64_t u = gp - __ldg(cup + lo);
         const int64_t L = __ldg(cu + lo + 1) - __ldg(cu + lo);
         l2r[q] = u < L ? (int32_t)(__ldg(cu + lo) + u) : -1;
@@ -138,7 +149,11 @@ __global__ void pad_maps_kernel(const int32_t *__restrict__ cu, const int32_t *_
             const int mid = (lo + hi) >> 1;
             if (__ldg(cu + mid) <= g) lo = mid; else hi = mid;
         }
-        r2l[g] = __ldg(g2l_padded + __ldg(cup + lo) + (g - __ldg(cu + lo)));
+        const int64_t gp = __ldg(cup + lo) + (g - __ldg(cu + lo));
+        if constexpr (kCheckBounds) {
+            if (!in_bounds(lo >= 0 && lo < n && gp >= 0 && gp < Tpad)) continue;
+        }
+        r2l[g] = __ldg(g2l_padded + gp);
     }
 }
 
@@ -175,6 +190,11 @@ __global__ void real_lengths_kernel(int layout, int P, const int32_t *__restrict
 }
 
 }  // namespace
+
+cudaError_t read_index_map_bounds_violations(unsigned int *count, bool reset)
+{
+    return read_bounds_counter(count, reset);
+}
 
 cudaError_t launch_index_map(int layout, int cp_size, const int32_t *cu, int n_docs, int64_t T,
                              int32_t *l2g, int32_t *g2l, cudaStream_t stream)

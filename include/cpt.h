@@ -593,6 +593,27 @@ CPT_API cpt_status cpt_epoch_status(const cpt_epoch *ep, int32_t owner, void *st
  *  Errors: CPT_ERR_INVALID_ARG (NULL count), CPT_ERR_DEVICE, CPT_ERR_CUDA. */
 CPT_API cpt_status cpt_kernel_wait_timeouts(uint32_t *count, int32_t reset);
 
+/* Whether this library was built with CPT_CHECK_BOUNDS (1) or not (0); the
+ * pages have no counterpart. The build of context_attention_token_gb300
+ * makes both: libcpt.so without the checks and libcpt_checked.so with them.
+ * Host only. */
+CPT_API int32_t cpt_bounds_checked(void);
+
+/* Failed device bounds checks since the last reset (the pages have no
+ * counterpart: it is this implementation's debug report). In a build with
+ * CPT_CHECK_BOUNDS every index a kernel reads from memory (an ownership-map
+ * entry, a document boundary) or derives from one (a rank, a local row) is
+ * checked against the extent of the buffer it addresses before it is used.
+ * A failed check adds one here and the access is skipped: the row is not
+ * read (the gather writes it as zeros) or not written. Nothing traps. A
+ * non-zero count means some earlier output is not valid. Valid inputs never
+ * fail a check.
+ *  count  host, receives the count.  reset  non-zero: zero it after reading.
+ *  Blocking: reads device memory synchronously.
+ *  Errors: CPT_ERR_UNSUPPORTED in a build without CPT_CHECK_BOUNDS;
+ *  CPT_ERR_INVALID_ARG (NULL count), CPT_ERR_DEVICE, CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_bounds_violations(uint32_t *count, int32_t reset);
+
 /* Test switch for the failure path of the bulk-copy kernels (the pages have no
  * counterpart). While on, every bulk-copy mbarrier of later launches on the
  * current device announces 16 bytes more than its copies deliver. Every
@@ -625,6 +646,33 @@ CPT_API cpt_status cpt_test_stall_bulk_waits(int32_t on);
 CPT_API cpt_status cpt_slot_reduce(const void *const *slots, int32_t n_slots, int64_t n_elems,
                            cpt_dtype in, cpt_dtype out, void *dst, const int32_t *status,
                            void *stream);
+
+/* ------------------------------------------------------------------ */
+/* Measurement                                                         */
+/* ------------------------------------------------------------------ */
+
+/* Streaming ceiling for a roofline (the pages have no counterpart; it
+ * computes nothing of the method). It moves the traffic of an HBM-bound call
+ * with no arithmetic and no index: dst receives a copy of srcs[0], and
+ * srcs[1..n_src) are read at the same offsets and discarded. With n_src = P
+ * the reads and writes are those of the fused gradient return (P writer
+ * rows in, one owner row out); with n_src = 1 they are those of the row
+ * gather (one row in, one out). The SM's bulk-copy engine moves blocks of
+ * block_bytes from every source into shared memory through a ring of
+ * `stages` stages, one issuing thread per CTA and at most ctas_per_sm CTAs
+ * per SM, and writes each block back with one bulk store, so the time
+ * measures the memory system for that read/write mix.
+ *  srcs         host array of n_src (1..8) device pointers, `bytes` each.
+ *  dst          device, `bytes`; must not overlap a source.
+ *  bytes        a multiple of 16 (0: nothing is launched).
+ *  block_bytes  a multiple of 16; n_src * block_bytes * stages <= 200 KB.
+ *  stages       2..8.  ctas_per_sm  1..32 (capped by occupancy).
+ *  Bulk-copy waits that run out are counted by cpt_kernel_wait_timeouts.
+ *  Errors: CPT_ERR_INVALID_ARG, CPT_ERR_ALIGNMENT, CPT_ERR_DEVICE,
+ *  CPT_ERR_ALIAS, CPT_ERR_CUDA. */
+CPT_API cpt_status cpt_stream_ceiling(const void *const *srcs, int32_t n_src, void *dst, int64_t bytes,
+                                      int32_t block_bytes, int32_t stages, int32_t ctas_per_sm,
+                                      void *stream);
 
 #ifdef __cplusplus
 }

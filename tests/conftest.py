@@ -25,13 +25,20 @@ def oracle_lib():
 
 @pytest.fixture(scope="session")
 def cpt():
-    """The C-ABI binding, built in-tree if missing or stale."""
+    """The C-ABI binding, built in-tree if missing or stale. Under
+    CPT_LIBRARY_VARIANT=checked it is the bounds-checked build, and the
+    session ends with a check that no device bounds check failed."""
     from context_attention_token_gb300 import build as cpt_build
 
     cpt_build.build()
     from context_attention_token_gb300 import cpt as binding
 
-    return binding
+    yield binding
+    import torch
+
+    if binding.cpt_bounds_checked() and torch.cuda.is_available() and torch.cuda.is_initialized():
+        torch.cuda.synchronize()
+        assert binding.cpt_bounds_violations() == 0, "a device bounds check failed during the session"
 
 
 @pytest.fixture(scope="session")

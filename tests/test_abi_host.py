@@ -186,3 +186,23 @@ def test_layout_padded_tokens_agrees_with_oracle(cpt, oracle_lib):
     with pytest.raises(cpt.CptError) as ei:
         cpt.cpt_layout_padded_tokens(PAD, 8, [0, 1, 2**31 - 8], 2**31 - 8)
     assert ei.value.status == cpt.CPT_ERR_INVALID_ARG
+
+
+def test_both_builds_export_every_declared_function(cpt):
+    """The release and the bounds-checked library export the same calls and
+    say which build they are."""
+    import ctypes
+
+    from context_attention_token_gb300 import build as cpt_build
+
+    declared = cpt.declared_functions(HEADER)
+    for variant, flag in (("release", 0), ("checked", 1)):
+        lib = ctypes.CDLL(cpt_build.library_path(variant))
+        missing = [n for n in declared if not hasattr(lib, n)]
+        assert not missing, (variant, missing)
+        lib.cpt_bounds_checked.restype = ctypes.c_int32
+        assert lib.cpt_bounds_checked() == flag, variant
+    if not cpt.cpt_bounds_checked():
+        with pytest.raises(cpt.CptError) as ei:
+            cpt.cpt_bounds_violations()
+        assert ei.value.status == cpt.CPT_ERR_UNSUPPORTED
