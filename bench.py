@@ -558,13 +558,22 @@ def run_config_rows(cpt, synth, stream, dev, peak, names, reps=20, warm=3, big=N
         wv = synth.device_normal_bf16((P, Tg, Hg, D), 7002, 1.0, dev)
         ok = torch.empty((P, Tg // P, Hg, D), dtype=torch.bfloat16, device=dev)
         ov = torch.empty_like(ok)
-        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        flush = torch.zeros(512 << 20, dtype=torch.uint8, device=dev)
+        sink = torch.empty((), dtype=torch.int64, device=dev)
+        nbytes = Tg * (2 * (P + 1) * rb + 2 * 4)
         ms = _events_ms(lambda: cpt.cpt_grad_return(plan, wk, wv, ok, ov), stream, reps, warm,
                         before=flush.zero_)
+        # the same after a flush that reads the 512 MB instead: L2 is then full
+        # of clean lines, and the launch pays no write-back of someone else's
+        ms_read = _events_ms(lambda: cpt.cpt_grad_return(plan, wk, wv, ok, ov), stream, reps, warm,
+                             before=lambda: torch.sum(flush.view(torch.int64), dim=0, out=sink))
+        gbs_read = nbytes / (ms_read / 1e3) / 1e9
         out["single_doc_grad_return_P4_S32768_8x128"] = row(
-            ms, Tg * (2 * (P + 1) * rb + 2 * 4), l2="flushed before each launch",
-            kernel=kernel_of(cpt.CPT_CALL_GRAD_RETURN, P, BF, BF, 0, rb, 2 * Tg))
-        del wk, wv, ok, ov, flush, plan
+            ms, nbytes, l2="flushed before each launch by writing 512 MB",
+            kernel=kernel_of(cpt.CPT_CALL_GRAD_RETURN, P, BF, BF, 0, rb, 2 * Tg),
+            read_flush={"ms": ms_read, "gbs": gbs_read, "frac_of_peak": gbs_read / peak,
+                        "l2": "flushed before each launch by reading 512 MB"})
+        del wk, wv, ok, ov, flush, sink, plan
 
     if "lognormal_partition" in names or "lognormal_grad_return" in names:
         # T=131072 from lognormal document lengths, 16x128 bf16: per-document
@@ -924,11 +933,9 @@ def run_gpu(args):
             link[key] = min(copies(inp, outp) for _ in range(2))
         r_in = h2d / (link["h2d_ms"] / 1e3)
         r_out = d2h / (link["d2h_ms"] / 1e3)
-        r_both = (h2d + d2h) / (link["both_ms"] / 1e3)
-        # even share: while both directions run, each gets half of the
-        # combined rate; the larger direction then finishes alone
-        lo, hi, r_hi = (d2h, h2d, r_in) if d2h <= h2d else (h2d, d2h, r_out)
-        link_floor_ms = (lo / (r_both / 2) + (hi - lo) / r_hi) * 1e3
+        # the floor of one step: all of its copies in and out at once, with
+        # nothing else on the link or the GPU
+        link_floor_ms = link["both_ms"]
 
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
         for i in range(2):  # warm-up: one step on each buffer set
@@ -954,6 +961,10 @@ def run_gpu(args):
         for h, d in zip(h_part + [h_dko, h_dvo], part + [dko, dvo]):
             if not torch.equal(flat(h)[rows_chk], flat(d)[rows_chk.to(dev)].cpu()):
                 raise RuntimeError("e2e results differ from the device-resident step")
+        # the same copies-only probe right after the leg (and its check): a
+        # link that was slow during the leg shows here too, a pipeline stall
+        # does not
+        both_after_ms = min(copies(True, True) for _ in range(2))
         del sets
         e2e = {"value": whole_job_gbs(step_bytes(S), 1, world, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -962,12 +973,14 @@ def run_gpu(args):
                             "two buffer sets so consecutive steps overlap"),
                "link_floor_ms": link_floor_ms,
                "vs_link_floor": e2e_ms / link_floor_ms,
-               "link": {"h2d_gbs": r_in / 1e9, "d2h_gbs": r_out / 1e9, "both_total_gbs": r_both / 1e9,
+               "link": {"h2d_gbs": r_in / 1e9, "d2h_gbs": r_out / 1e9,
+                        "h2d_alone_ms": link["h2d_ms"], "d2h_alone_ms": link["d2h_ms"],
                         "copies_only_ms": link["both_ms"],
-                        "how": ("the step's own pinned buffers copied in alone, out alone and both at "
-                                "once (best of 2, CUDA events) just before the e2e leg; floor = "
-                                "smaller direction at half the combined rate, then the rest of the "
-                                "larger direction alone")}}
+                        "copies_only_after_ms": both_after_ms,
+                        "how": ("the step's own pinned buffers copied in alone, out alone, and all "
+                                "in and out at once on two streams (best of 2, CUDA events), just "
+                                "before the e2e leg and again after it; link_floor_ms = the "
+                                "all-at-once time before the leg")}}
         del host_in, host_out
 
     if rank != 0:
@@ -1365,7 +1378,12 @@ def run_grad_return_size_sweep(args):
     peak, peak_src = load_peak()
     Hs = args.heads if args.heads != 20 else 8
     rb = Hs * D * 2
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flush = torch.zeros(512 << 20, dtype=torch.uint8, device="cuda")
+    sink = torch.empty((), dtype=torch.int64, device="cuda")
+    # "write" overwrites 512 MB (the flush the timing rules name), which leaves
+    # L2 full of dirty lines the next kernel has to write back; "read" sums the
+    # same 512 MB, which leaves it full of clean lines
+    do_flush = flush.zero_ if args.flush == "write" else (lambda: torch.sum(flush.view(torch.int64), dim=0, out=sink))
     sizes = (8192, 16384, 32768, 65536, 131072, 262144)
     data = {name: [] for name in ("auto", "loads", "bulk")}
     for Ts in sizes:
@@ -1379,12 +1397,13 @@ def run_grad_return_size_sweep(args):
                            ("bulk", cpt.CPT_KERNEL_BULK)):
             cpt.cpt_set_kernel_path(code)
             ms = _events_ms(lambda: cpt.cpt_grad_return(plan, wk, wv, ok, ov), stream, 20, 3,
-                            before=flush.zero_)
+                            before=do_flush)
             data[name].append((nbytes, ms))
             gbs = nbytes / (ms / 1e3) / 1e9
             print(json.dumps({"sweep": "grad_return_launch_size", "kernel": name, "P": P, "S": Ts,
                               "row_bytes": rb, "bytes": nbytes, "ms": ms, "gbs": gbs,
-                              "frac_of_peak": gbs / peak, "l2": "flushed before each launch"}), flush=True)
+                              "frac_of_peak": gbs / peak,
+                              "l2": f"flushed before each launch by a 512 MB {args.flush}"}), flush=True)
         cpt.cpt_set_kernel_path(cpt.CPT_KERNEL_AUTO)
         del wk, wv, ok, ov, plan
         torch.cuda.empty_cache()
@@ -1395,7 +1414,8 @@ def run_grad_return_size_sweep(args):
         sxx = sum((b - mx) ** 2 for b, _ in pts)
         slope = sum((b - mx) * (t - my) for b, t in pts) / sxx  # ms per byte
         t0 = my - slope * mx
-        print(json.dumps({"sweep": "grad_return_launch_size_fit", "kernel": name, "t0_us": t0 * 1e3,
+        print(json.dumps({"sweep": "grad_return_launch_size_fit", "kernel": name, "flush": args.flush,
+                          "t0_us": t0 * 1e3,
                           "streaming_gbs": 1 / (slope / 1e3) / 1e9,
                           "streaming_frac_of_peak": 1 / (slope / 1e3) / 1e9 / peak,
                           "peak": peak, "peak_source": peak_src,
@@ -1527,6 +1547,8 @@ def main():
                     help="kernel of the gradient return and the slot reduce: the measured rule "
                          "(default), or one forced")
     ap.add_argument("--slots", type=int, default=8, help="--sweep slot_reduce: number of slots (1..8)")
+    ap.add_argument("--flush", choices=["write", "read"], default="write",
+                    help="--sweep grad_return_sizes: flush L2 by writing or by reading 512 MB")
     ap.add_argument("--configs", default="all",
                     help="configuration rows timed after the step: all, none, or a comma list of "
                          + ", ".join(CONFIG_ROWS))
