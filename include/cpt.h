@@ -403,7 +403,10 @@ CPT_API cpt_status cpt_grad_return_accumulate(const cpt_plan *plan, const void *
  *  - CPT_KERNEL_BULK: data moves through shared memory with bulk copies.
  *    Row gather: blocks of up to 40 KB of consecutive rows, one bulk load
  *    per contiguous source run and one bulk store per rank piece; it needs
- *    4 blocks to fit in 200 KB. Gradient return: one owner row's P writer
+ *    4 blocks to fit in 200 KB. Where the map is the identity and each
+ *    tensor's rank pieces lie end to end in one buffer (packed-contiguous
+ *    partition and restore), the same choice runs a straight copy of 32 KB
+ *    blocks instead, with no map. Gradient return: one owner row's P writer
  *    rows per warp (and, for cpt_grad_return_accumulate, the owner's current
  *    row); it needs 2 x (P x input row + output row) bytes of at most
  *    112 KB. Slot reduce: 4 KB of every slot per warp; it needs equal input

@@ -7,7 +7,11 @@ oracle, with canary bands around every output. The cases exercise the
 blocks kernel's paths: one contiguous source run per block (large
 documents), several runs per block (many short documents), zero-filled
 padding rows (padded layout), blocks split across two rank pieces (row
-ranges), and rows at and just past its shared-memory limit.
+ranges), and rows at and just past its shared-memory limit. Where the map is
+the identity and the destination contiguous (packed-contiguous partition,
+restore and scatter), the bulk path is a straight copy: those cases cover a
+ring that wraps many times, a short last block, row ranges and slots that
+are not contiguous.
 """
 import numpy as np
 import pytest
@@ -47,6 +51,8 @@ CASES = [
     (PACKED, 8, [0, 77, 19], 640, "f32"),
     (PADDED, 4, [5, 33, 1, 12], 2560, "bf16"),          # zero-filled padding rows
     (PADDED, 8, [3, 17, 100], 512, "f32"),
+    (PACKED, 4, [70000, 60000, 1072], 512, "bf16"),     # straight copy: 4096 blocks, the ring wraps
+    (PACKED, 2, [7, 9], 8, "bf16"),                     # straight copy of 16-byte rows, one short block
 ]
 
 
@@ -88,7 +94,7 @@ def test_partition_and_restore_both_kernels(cpt, cuda_device, kernel, case):
         assert g.bands_intact() and bk.bands_intact()
 
 
-@pytest.mark.parametrize("case", [CASES[0], CASES[1], CASES[5], CASES[12]], ids=_ids)
+@pytest.mark.parametrize("case", [CASES[0], CASES[1], CASES[5], CASES[10], CASES[12], CASES[14]], ids=_ids)
 def test_partition_row_ranges_both_kernels(cpt, cuda_device, kernel, case):
     """Ranges that start and end inside rank pieces, so blocks straddle two
     ranks, and a range of one row."""
@@ -107,6 +113,31 @@ def test_partition_row_ranges_both_kernels(cpt, cuda_device, kernel, case):
     torch.cuda.synchronize()
     for w, pc in zip(whole, pieces):
         assert np.array_equal(bits(to_host(w)), bits(to_host(pc)))
+
+
+@pytest.mark.parametrize("contiguous", [True, False])
+def test_packed_scatter_into_slots(cpt, cuda_device, kernel, contiguous):
+    """The staged scatter with the identity map: slots laid end to end make
+    it a straight copy, separate slots keep it a gather; both give the
+    oracle's slots."""
+    P, lens, row = 4, [70000, 61072], 512
+    cu = synth.cu_from_lengths(lens)
+    T = int(cu[-1])
+    plan = cpt.cpt_plan_create(PACKED, P, cu, T)
+    x = synth.uniform_bf16(np.random.default_rng(9300), (T, row))
+    if contiguous:
+        buf = torch.empty((P, T // P, row), dtype=torch.bfloat16, device="cuda")
+        slots = [buf[o] for o in range(P)]
+    else:  # 16 rows of gap between slots, so they are never laid end to end
+        buf = torch.empty((P, T // P + 16, row), dtype=torch.bfloat16, device="cuda")
+        slots = [buf[o, : T // P] for o in range(P)]
+    w = 1
+    cpt.cpt_grad_scatter(plan, w, to_dev(x), slots, slots[w])
+    torch.cuda.synchronize()
+    l2g, _ = oracle.index_map(PACKED, P, cu, T)
+    want = oracle.grad_scatter(l2g, x, P)
+    for o in range(P):
+        assert np.array_equal(to_host(slots[o]), want[o])
 
 
 def test_no_gather_wait_ran_out(cpt, cuda_device):
