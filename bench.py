@@ -862,11 +862,16 @@ def run_gpu(args):
             # read them (two steps back) are done, and its outputs only after
             # they were copied out.
             s_qkv, s_dkw, s_dvw, s_part, s_dko, s_dvo = sets[i % 2]
+            t_host = time.perf_counter()
             plan = cpt.cpt_plan_create(cpt.CPT_LAYOUT_DUAL_CHUNK_SWAP, P, cu, S, workspace=ws)
             if kernels_done[i % 2] is not None:
                 h2d_stream.wait_event(kernels_done[i % 2])
             if outputs_out[i % 2] is not None:
                 stream.wait_event(outputs_out[i % 2])
+            # diagnostics: when this step's copies in start and end, and when
+            # its copies out end, on their own streams
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            marks[0].record(h2d_stream)
             for g0, q0, c in pieces:
                 with torch.cuda.stream(h2d_stream):
                     for d, h in zip(s_qkv, h_qkv):
@@ -893,11 +898,16 @@ def run_gpu(args):
                     d2h_stream.wait_event(grads_done)
                     flat(h_dko)[q0:q0 + c].copy_(flat(s_dko)[q0:q0 + c], non_blocking=True)
                     flat(h_dvo)[q0:q0 + c].copy_(flat(s_dvo)[q0:q0 + c], non_blocking=True)
+            marks[1].record(h2d_stream)
+            marks[2].record(d2h_stream)
             kernels_done[i % 2] = torch.cuda.Event()
             kernels_done[i % 2].record(stream)
             outputs_out[i % 2] = torch.cuda.Event()
             outputs_out[i % 2].record(d2h_stream)
             cpt.cpt_plan_destroy(plan)
+            step_marks.append((marks, (time.perf_counter() - t_host) * 1e3))
+
+        step_marks = []
 
         def join():
             stream.wait_stream(h2d_stream)
@@ -942,6 +952,7 @@ def run_gpu(args):
             e2e_step(i)
         join()
         torch.cuda.synchronize()
+        step_marks.clear()
         if world > 1:
             dist.barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -954,6 +965,15 @@ def run_gpu(args):
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(a.elapsed_time(b), dev) / e2e_steps
+        # per step: copies-in span, idle time of the copy-in stream before the
+        # step's first copy, lag of the last copy out behind the last copy in,
+        # and host time to enqueue the step (large when the host had to wait)
+        spans = [m[0].elapsed_time(m[1]) for m, _ in step_marks]
+        gaps = [step_marks[k - 1][0][1].elapsed_time(step_marks[k][0][0]) for k in range(1, len(step_marks))]
+        lags = [m[1].elapsed_time(m[2]) for m, _ in step_marks]
+        host = [h for _, h in step_marks]
+        diag = {"h2d_span_ms": [round(x, 2) for x in spans], "h2d_idle_before_ms": [round(x, 2) for x in gaps],
+                "d2h_lag_ms": [round(x, 2) for x in lags], "host_enqueue_ms": [round(x, 2) for x in host]}
         # the results that came back equal the device-resident step's, on
         # sampled rows of every output (both sets computed the same inputs)
         g = torch.Generator().manual_seed(7)
@@ -971,6 +991,7 @@ def run_gpu(args):
                "steps": e2e_steps,
                "pipeline": (f"copies in, kernels, copies out on 3 streams over {len(pieces)} pieces, "
                             "two buffer sets so consecutive steps overlap"),
+               "diag": diag,
                "link_floor_ms": link_floor_ms,
                "vs_link_floor": e2e_ms / link_floor_ms,
                "link": {"h2d_gbs": r_in / 1e9, "d2h_gbs": r_out / 1e9,
