@@ -361,7 +361,7 @@ int block_rows(int64_t row_bytes)
 // tensor's rank pieces laid end to end in one destination buffer.
 bool is_straight_copy(const GatherParams &p)
 {
-    if (p.l2g != nullptr) return false;
+    if (p.l2g != nullptr || p.parts < 1) return false;
     const int nt = (int)(p.rows / p.T);
     for (int t = 0; t < nt; ++t)
         for (int r = 1; r < p.parts; ++r)
