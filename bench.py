@@ -476,6 +476,7 @@ def _events_ms(fn, stream, reps, warm, before=None):
 CEILING_SHAPES = {
     "read4_write1": [(10240, 4, 1), (8192, 4, 1), (12288, 4, 1), (5120, 4, 2), (5120, 8, 1), (16384, 3, 1)],
     "read1_write1": [(32768, 4, 1), (40960, 4, 1), (16384, 4, 2), (8192, 4, 2), (32768, 3, 1), (24576, 8, 1)],
+    "read8_write1": [(4096, 4, 1), (8192, 3, 1), (4096, 6, 1), (2048, 4, 2), (3072, 8, 1)],
 }
 
 
@@ -625,7 +626,21 @@ def run_config_rows(cpt, synth, stream, dev, peak, names, reps=20, warm=3, big=N
                 kern = kernel_of(cpt.CPT_CALL_SLOT_REDUCE, n_slots, code, code, 0, nbytes, 0)
                 if nbytes >= 1 << 30:
                     ms = _events_ms(lambda: cpt.cpt_slot_reduce(slots, dst), stream, 10, warm)
-                    out[f"slot_reduce_8x{label}_{tag}"] = row(ms, (n_slots + 1) * nbytes, kernel=kern)
+                    r = row(ms, (n_slots + 1) * nbytes, kernel=kern)
+                    # the ceiling with the same 8 reads : 1 write, once per run
+                    if "read8_write1" not in out.setdefault("_ceilings", {}):
+                        tried = []
+                        for blk, stages, ctas in CEILING_SHAPES["read8_write1"]:
+                            c_ms = _events_ms(lambda: cpt.cpt_stream_ceiling(slots, dst, blk, stages, ctas),
+                                              stream, 10, warm)
+                            tried.append(((n_slots + 1) * nbytes / (c_ms / 1e3) / 1e9, blk, stages, ctas))
+                        best = max(tried)
+                        out["_ceilings"]["read8_write1"] = {
+                            "gbs": best[0], "shape": {"block_bytes": best[1], "stages": best[2],
+                                                      "ctas_per_sm": best[3]},
+                            "tried_gbs": [round(t[0], 1) for t in tried]}
+                    r["frac_mix"] = r["gbs"] / out["_ceilings"]["read8_write1"]["gbs"]
+                    out[f"slot_reduce_8x{label}_{tag}"] = r
                 else:
                     iters = 200
                     launched = _events_ms(lambda: [cpt.cpt_slot_reduce(slots, dst) for _ in range(iters)],
@@ -1061,7 +1076,8 @@ def run_gpu(args):
                      "peak_mix": ceil["read4_write1"]["gbs"],
                      "traffic": traffic if PATH == "fused" else None,
                      "traffic_source": traffic_note if PATH == "fused" else None},
-        "ceilings": {**ceil, "how": ("cpt_stream_ceiling: the read/write mix of the call with no "
+        "ceilings": {**ceil, **configs.pop("_ceilings", {}),
+                     "how": ("cpt_stream_ceiling: the read/write mix of the call with no "
                                      "arithmetic, bulk copies through shared memory; the fastest of "
                                      "the shapes tried, CUDA events, median of 10 after 3")},
         "configs": configs,
