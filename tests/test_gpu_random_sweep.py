@@ -120,6 +120,7 @@ def _run_case(cpt, seed, case):
         cup, meta_layout, meta_cu = cu, layout, cu
     Tpad = int(cup[-1])
     assert plan.padded_tokens == Tpad
+    assert cpt.cpt_layout_padded_tokens(layout, P, cu, T) == Tpad  # the host query agrees with the plan
 
     # maps, metadata, real lengths
     d_l2g = torch.empty(Tpad, dtype=torch.int32, device="cuda")
