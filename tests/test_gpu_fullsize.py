@@ -222,3 +222,61 @@ def test_slot_reduce_one_gigabyte_slots_whole_output(cpt, cuda_device, dtype):
     want = _oracle_slot_reduce_chunked(hs, oracle.BF16 if dtype == torch.bfloat16 else oracle.F32,
                                        min(16, _host_threads()))
     assert np.array_equal(bits(got), bits(want))
+
+
+def test_packed_partition_and_restore_pages_shape_whole_output(cpt, cuda_device):
+    """The packed-contiguous policy at the pages' shape (P=4, S=262144, one
+    document, 20x128 bf16): the whole Q/K/V partition against the oracle's
+    packed map, and the restore back to the inputs. At this size the bulk path
+    runs its straight copy."""
+    cu = np.array([0, S], np.int32)
+    plan = cpt.cpt_plan_create(1, P, cu, S)
+    l2g, _ = oracle.index_map(1, P, cu, S)
+    qkv = [synth.device_normal_bf16((S, H, D), 4020 + t, 1.0, "cuda") for t in range(3)]
+    dst = [torch.empty((P, TP, H, D), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    cpt.cpt_partition(plan, qkv, dst)
+    torch.cuda.synchronize()
+    for x, d in zip(qkv, dst):
+        assert np.array_equal(to_host(d).reshape(S, H, D), oracle.partition(l2g, to_host(x)))
+    back = [torch.empty((S, H, D), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    cpt.cpt_restore(plan, dst, back)
+    torch.cuda.synchronize()
+    for x, b in zip(qkv, back):
+        assert torch.equal(b.view(torch.int16), x.view(torch.int16))
+    assert cpt.cpt_kernel_wait_timeouts() == 0
+    del qkv, dst, back
+    torch.cuda.empty_cache()
+
+
+def test_staged_path_equals_fused_pages_shape(cpt, big_plan):
+    """The staged gradient return at the pages' shape (P writer streams
+    scatter into owner slots and publish an epoch, P owner streams wait and
+    reduce their slots in writer order) equals the fused launch bit for bit;
+    the fused launch equals the oracle on every element (above)."""
+    plan, _ = big_plan
+    dkw = synth.device_normal_bf16((P, S, H, D), 4001, 0.02, "cuda")
+    fused = torch.empty((P, TP, H, D), dtype=torch.bfloat16, device="cuda")
+    cpt.cpt_grad_return(plan, dkw, None, fused, None)
+    slots = torch.empty((P, P, TP, H, D), dtype=torch.bfloat16, device="cuda")
+    staged = torch.full((P, TP, H, D), 9.0, dtype=torch.bfloat16, device="cuda")
+    ep = cpt.cpt_epoch_create(P)
+    main = torch.cuda.current_stream()
+    wst = [torch.cuda.Stream() for _ in range(P)]
+    ost = [torch.cuda.Stream() for _ in range(P)]
+    cpt.cpt_epoch_advance(ep)
+    for w in range(P):
+        wst[w].wait_stream(main)
+        cpt.cpt_grad_scatter(plan, w, dkw[w], [slots[o, w] for o in range(P)], slots[w, w], stream=wst[w])
+        cpt.cpt_epoch_publish(ep, w, stream=wst[w])
+    for o in range(P):
+        ost[o].wait_stream(main)
+        cpt.cpt_epoch_wait(ep, o, 2_000_000_000, cpt.CPT_WAIT_BOUNDED, stream=ost[o])
+        cpt.cpt_slot_reduce(slots[o], staged[o], ep.status_ptr(o), stream=ost[o])
+    for st in wst + ost:
+        main.wait_stream(st)
+    torch.cuda.synchronize()
+    assert [cpt.cpt_epoch_status(ep, o) for o in range(P)] == [0] * P
+    assert torch.equal(staged.view(torch.int16), fused.view(torch.int16))
+    assert cpt.cpt_kernel_wait_timeouts() == 0
+    del dkw, fused, slots, staged
+    torch.cuda.empty_cache()
