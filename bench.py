@@ -19,6 +19,7 @@ on a bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -645,6 +646,16 @@ def run_config_rows(cpt, synth, stream, dev, peak, names, reps=20, warm=3, big=N
                     iters = 200
                     launched = _events_ms(lambda: [cpt.cpt_slot_reduce(slots, dst) for _ in range(iters)],
                                           stream, 3, 1) * 1e3 / iters
+                    # the same call straight through the C ABI with its arguments
+                    # built once, as a C or C++ caller makes it: the library's
+                    # own host cost (checks and launch) without the binding's
+                    arr = (ctypes.c_void_p * n_slots)(*[x.data_ptr() for x in slots])
+                    c_args = (ctypes.cast(arr, ctypes.c_void_p), n_slots, n, code, code,
+                              ctypes.c_void_p(dst.data_ptr()), None, ctypes.c_void_p(stream.cuda_stream))
+                    if cpt._lib.cpt_slot_reduce(*c_args) != cpt.CPT_OK:
+                        raise RuntimeError(cpt.cpt_last_error_string())
+                    c_abi = _events_ms(lambda: [cpt._lib.cpt_slot_reduce(*c_args) for _ in range(iters)],
+                                       stream, 3, 1) * 1e3 / iters
                     side = torch.cuda.Stream(device=dev)
                     side.wait_stream(stream)
                     g = torch.cuda.CUDAGraph()
@@ -654,9 +665,12 @@ def run_config_rows(cpt, synth, stream, dev, peak, names, reps=20, warm=3, big=N
                     stream.wait_stream(side)
                     graph_us = _events_ms(g.replay, stream, 3, 1) * 1e3 / iters
                     out[f"slot_reduce_8x{label}_{tag}"] = {
-                        "us_per_call_launched": launched, "us_per_call_graph": graph_us,
+                        "us_per_call_launched": launched, "us_per_call_c_abi": c_abi,
+                        "us_per_call_graph": graph_us,
                         "bytes": (n_slots + 1) * nbytes, "kernel": kern,
-                        "note": "latency: L2-resident, back-to-back calls"}
+                        "note": ("latency, L2-resident, back-to-back calls: launched = through the "
+                                 "Python binding; c_abi = the C entry point with prebuilt arguments; "
+                                 "graph = replays of a CUDA graph of such calls")}
                     del g
                 del slots, dst
 
