@@ -183,9 +183,17 @@ def _ptr(t) -> int:
     return t.data_ptr()
 
 
+# ctypes array types of n device pointers, built once per n
+_PTR_ARRAYS = {}
+
+
 def _ptr_array(items):
-    arr = (_vp * len(items))(*[_ptr(x) for x in items])
-    return arr
+    """Device pointers of the items as a C array (passed by its address)."""
+    n = len(items)
+    kind = _PTR_ARRAYS.get(n)
+    if kind is None:
+        kind = _PTR_ARRAYS.setdefault(n, _vp * n)
+    return kind(*[_ptr(x) for x in items])
 
 
 class _Parts:
@@ -211,16 +219,30 @@ class _Parts:
             t = list(t)
             if len(t) != parts:
                 raise ValueError(f"expected {parts} tensors, got {len(t)}")
-            for x in t[1:]:
-                if tuple(x.shape) != tuple(t[0].shape) or x.dtype != t[0].dtype:
+            first = t[0]
+            shape, dtype = first.shape, first.dtype
+            ptrs = []
+            for x in t:
+                if isinstance(x, int):
+                    raise TypeError("parts must be tensors")
+                if x.shape != shape or x.dtype != dtype:
                     raise ValueError("the parts differ in shape or dtype")
-            self.ptrs = [_ptr(x) for x in t]
-            self.shape = tuple(t[0].shape)
-            self.dtype = t[0].dtype
-            self.part_bytes = _nbytes(t[0])
+                if not x.is_contiguous():
+                    raise ValueError("tensors must be contiguous")
+                ptrs.append(x.data_ptr())
+            self.ptrs = ptrs
+            self.shape = tuple(shape)
+            self.dtype = dtype
+            self.part_bytes = first.numel() * first.element_size()
 
     def array(self):
-        return ctypes.cast((_vp * len(self.ptrs))(*self.ptrs), _vp)
+        """The pointers as a C array; ctypes passes an array argument by its
+        address, and the call keeps the array alive while it runs."""
+        n = len(self.ptrs)
+        kind = _PTR_ARRAYS.get(n)
+        if kind is None:
+            kind = _PTR_ARRAYS.setdefault(n, _vp * n)
+        return kind(*self.ptrs)
 
     def row_elems(self) -> int:
         n = 1
@@ -390,8 +412,8 @@ def cpt_partition(plan: Plan, srcs, dsts, stream=None):
     """dsts[t] ([P, T/P, ...]) = rank-local reorder of srcs[t] ([T, ...])."""
     srcs, dsts = list(srcs), list(dsts)
     _check_gather(plan, srcs, dsts, plan.total_tokens, plan.padded_tokens, _row_elems(srcs[0]) if srcs else 0)
-    _check(_lib.cpt_partition(plan.handle, len(srcs), ctypes.cast(_ptr_array(srcs), _vp),
-                              ctypes.cast(_ptr_array(dsts), _vp), _row_elems(srcs[0]), _dtype_code(srcs[0]),
+    _check(_lib.cpt_partition(plan.handle, len(srcs), _ptr_array(srcs),
+                              _ptr_array(dsts), _row_elems(srcs[0]), _dtype_code(srcs[0]),
                               _stream(stream)))
 
 
@@ -399,8 +421,8 @@ def cpt_partition_rows(plan: Plan, srcs, dsts, local_begin: int, local_count: in
     """cpt_partition for flattened local rows [local_begin, local_begin + local_count) only."""
     srcs, dsts = list(srcs), list(dsts)
     _check_gather(plan, srcs, dsts, plan.total_tokens, plan.padded_tokens, _row_elems(srcs[0]) if srcs else 0)
-    _check(_lib.cpt_partition_rows(plan.handle, len(srcs), ctypes.cast(_ptr_array(srcs), _vp),
-                                   ctypes.cast(_ptr_array(dsts), _vp), _row_elems(srcs[0]),
+    _check(_lib.cpt_partition_rows(plan.handle, len(srcs), _ptr_array(srcs),
+                                   _ptr_array(dsts), _row_elems(srcs[0]),
                                    _dtype_code(srcs[0]), local_begin, local_count, _stream(stream)))
 
 
@@ -408,8 +430,8 @@ def cpt_restore(plan: Plan, srcs, dsts, stream=None):
     """dsts[t] ([T, ...]) = global-order copy of the rank-local srcs[t] ([P, T/P, ...])."""
     srcs, dsts = list(srcs), list(dsts)
     _check_gather(plan, srcs, dsts, plan.padded_tokens, plan.total_tokens, _row_elems(dsts[0]) if dsts else 0)
-    _check(_lib.cpt_restore(plan.handle, len(srcs), ctypes.cast(_ptr_array(srcs), _vp),
-                            ctypes.cast(_ptr_array(dsts), _vp), _row_elems(dsts[0]),
+    _check(_lib.cpt_restore(plan.handle, len(srcs), _ptr_array(srcs),
+                            _ptr_array(dsts), _row_elems(dsts[0]),
                             _dtype_code(srcs[0]), _stream(stream)))
 
 
