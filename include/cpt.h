@@ -45,17 +45,19 @@
  *               non-zero cpt_status and cpt_last_error_string() explains it.
  *               Device-side failures go to device memory the host reads:
  *               an epoch wait timeout to a status word, a bulk-copy wait
- *               that ran out to a counter (cpt_kernel_wait_timeouts).
- *               Nothing aborts or traps.
+ *               that ran out to a counter (cpt_kernel_wait_timeouts), and
+ *               in the bounds-checked build a failed index check to another
+ *               (cpt_bounds_violations). Nothing aborts or traps.
  *   Threads     Calls are thread-safe; the error string is per thread.
  *   Graphs      cpt_index_map, cpt_thd_metadata, cpt_thd_real_lengths,
  *               cpt_partition, cpt_restore, cpt_grad_return(_accumulate),
  *               cpt_grad_scatter and cpt_slot_reduce only enqueue kernels, so
  *               they can be recorded into a CUDA graph (build the plan
- *               first). cpt_plan_create and the epoch publish/wait calls act
- *               on host state at call time and return CPT_ERR_UNSUPPORTED
- *               inside stream capture (as the pages' experimental CP path
- *               rejects graph capture, [TE-3221] "Scope and constraints").
+ *               first). cpt_plan_create, cpt_grad_return_noalloc and the
+ *               epoch publish/wait calls act on host state at call time and
+ *               return CPT_ERR_UNSUPPORTED inside stream capture (as the
+ *               pages' experimental CP path rejects graph capture, [TE-3221]
+ *               "Scope and constraints").
  *   Layout      A "row" is the H*D elements of one token. Global tensors are
  *               [T][row]. A rank-major local tensor is [P][T/P][row]: rank
  *               r's j-th local token is flattened local index q = r*T/P + j.
