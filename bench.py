@@ -1515,6 +1515,21 @@ def run_slot_reduce_sweep(args):
                 b.record(stream)
             torch.cuda.synchronize()
             call_us = a.elapsed_time(b) * 1e3 / iters
+            # the same call straight through the C ABI, arguments built once
+            arr = (ctypes.c_void_p * n_slots)(*[x.data_ptr() for x in slots])
+            code = cpt.CPT_F32 if dtype == torch.float32 else cpt.CPT_BF16
+            c_args = (arr, n_slots, n, code, code, ctypes.c_void_p(dst.data_ptr()), None,
+                      ctypes.c_void_p(stream.cuda_stream))
+            if cpt._lib.cpt_slot_reduce(*c_args) != cpt.CPT_OK:
+                raise RuntimeError(cpt.cpt_last_error_string())
+            with torch.cuda.stream(stream):
+                a1, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a1.record(stream)
+                for _ in range(iters):
+                    cpt._lib.cpt_slot_reduce(*c_args)
+                b1.record(stream)
+            torch.cuda.synchronize()
+            c_abi_us = a1.elapsed_time(b1) * 1e3 / iters
             # the same calls captured once into a graph and replayed
             graph_us = None
             g_iters = min(iters, 200)
@@ -1552,7 +1567,8 @@ def run_slot_reduce_sweep(args):
                     "dtype": "f32" if dtype == torch.float32 else "bf16", "slots": n_slots,
                     "kernel_path": args.kernel_path,
                     "bytes_per_slot": nbytes, "iters": iters,
-                    "us_per_call_launched": call_us, "us_per_call_graph": graph_us,
+                    "us_per_call_launched": call_us, "us_per_call_c_abi": c_abi_us,
+                    "us_per_call_graph": graph_us,
                     "us_per_call_cold_l2": cold_us,
                     "l2_resident_when_repeated": (n_slots + 1) * nbytes < 129 * 2**20,
                     "gbs": gbs, "frac_of_peak": gbs / peak, "peak": peak, "peak_source": peak_src}
